@@ -1,0 +1,279 @@
+/*
+ * dsvit.h — C ABI of the GB300 (sm_103a) vision-tower encode.
+ *
+ * The encode turns uint8 RGB pixels into language-space image tokens:
+ * 14x14 patchify + CLIP normalisation + patch projection, a pre-LayerNorm ViT
+ * (hidden 1024, 16 heads of 64, raw patch-grid 2D RoPE, bf16 activations at
+ * every stored boundary), a final LayerNorm, the 3x3 spatial merge and the two
+ * merger linears to width 5120; then the row-major image token span and the
+ * overlay of the embeddings onto the prompt's hidden-state rows.
+ *
+ * Sources (cited by page title and section):
+ *   [A] "DeepSeek V4.1 Flash Engineering, Part 3: Integrating Vision" (zLLM).
+ *   [B] ds4-learning glossary, "vision" (V4.1 Flash vision paragraph, family table).
+ *   [C] Lucebox "Image input" (DS4V section: failed encodes publish nothing partial).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are caller-owned.  "device" pointers are CUDA device (or managed)
+ *     memory on the current device; "host" pointers are CPU memory.
+ *   - bf16 tensors are row-major with the stated shapes; every device pointer
+ *     must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Launching entry points are asynchronous on that stream.
+ *   - Return value: DS_VIT_OK (0) or a negative DS_VIT_E* code.  All argument
+ *     checks run before the first launch; on an error nothing has been written
+ *     ([C], DS4V: a failed encode publishes no partial embedding matrices).
+ *   - Every spin-wait inside a kernel gives up after about two seconds, records
+ *     DS_VIT_ETIMEOUT in a device status word and returns; read it with
+ *     ds_vit_device_status (or, for the ds_vit_op_* calls, from `status`).
+ */
+#ifndef DSVIT_H
+#define DSVIT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS_VIT_OK 0
+#define DS_VIT_EINVAL (-1)   /* null pointer, bad size, unsupported config */
+#define DS_VIT_ERANGE (-2)   /* an image over the patch/token limits, a row outside the buffer */
+#define DS_VIT_ECAP (-3)     /* an output capacity or the workspace is too small */
+#define DS_VIT_ECUDA (-4)    /* a CUDA runtime / driver call failed */
+#define DS_VIT_ETIMEOUT (-5) /* a kernel's bounded wait gave up (device status word) */
+#define DS_VIT_ENOMEM (-6)   /* ds_vit_prepare could not allocate its device copies */
+
+#define DS_VIT_MAX_LAYERS 32
+#define DS_VIT_MAX_IMAGES 64       /* images per batch call */
+#define DS_VIT_MAX_PATCHES 9216    /* patches of one image (96 x 96 grid) */
+#define DS_VIT_MAX_TOKENS 1024     /* merged tokens of one image ([A] Step 1) */
+
+/* Row types of the image token span ([A] "Connect the complete image-to-text path first"). */
+#define DS_VIT_TOK_START 0
+#define DS_VIT_TOK_IMAGE 1
+#define DS_VIT_TOK_NEWLINE 2
+#define DS_VIT_TOK_END 3
+
+/* Epilogues of ds_vit_op_linear. */
+#define DS_VIT_EPI_BIAS 0        /* out = bf16(a w^T + bias) */
+#define DS_VIT_EPI_BIAS_GELU 1   /* out = bf16(gelu_erf(a w^T + bias)) */
+#define DS_VIT_EPI_BIAS_RESID 2  /* out = bf16(out + (a w^T + bias))   (in place) */
+#define DS_VIT_EPI_QKV_ROPE 3    /* N = 3072: q, k rotated by 2D RoPE, then bf16 */
+
+/* Model constants.  Only hidden 1024, heads 16, head_dim 64, mlp 4096,
+ * out_dim 5120, patch 14 and merge 3 are supported; n_layers 1..32. */
+typedef struct ds_vit_config {
+  int32_t n_layers;
+  int32_t hidden;
+  int32_t heads;
+  int32_t head_dim;
+  int32_t mlp;
+  int32_t out_dim;
+  int32_t patch;
+  int32_t merge;
+  float rope_theta;      /* 10000 */
+  float ln_eps;          /* 1e-6 */
+  float mean[3];         /* pixel mean per channel (CLIP) */
+  float std[3];          /* pixel std per channel (CLIP) */
+  int32_t image_token_id;
+} ds_vit_config;
+
+/* One ViT block's weights: device bf16, nn.Linear layout [out, in]. */
+typedef struct ds_vit_layer_weights {
+  const void *ln1_g, *ln1_b;     /* [1024] */
+  const void *qkv_w, *qkv_b;     /* [3072, 1024], [3072]; rows: q (head h at h*64), k, v */
+  const void *proj_w, *proj_b;   /* [1024, 1024], [1024] */
+  const void *ln2_g, *ln2_b;     /* [1024] */
+  const void *fc1_w, *fc1_b;     /* [4096, 1024], [4096] */
+  const void *fc2_w, *fc2_b;     /* [1024, 4096], [1024] */
+} ds_vit_layer_weights;
+
+/* All weights: device bf16. */
+typedef struct ds_vit_weights {
+  const void *patch_w, *patch_b; /* [1024, 588], input index c*196 + y*14 + x; [1024] */
+  ds_vit_layer_weights layers[DS_VIT_MAX_LAYERS];
+  const void *lnm_g, *lnm_b;     /* final (merger) LayerNorm [1024] */
+  const void *m1_w, *m1_b;       /* [5120, 9216], input index c*9 + dy*3 + dx; [5120] */
+  const void *m2_w, *m2_b;       /* [5120, 5120], [5120] */
+  const void *sentinel;          /* [3, 5120]: START, NEWLINE, END vectors */
+} ds_vit_weights;
+
+typedef struct ds_vit_prepared ds_vit_prepared;
+
+/* One image span for ds_vit_overlay. */
+typedef struct ds_vit_span {
+  int64_t base_row;     /* destination row of the span's first (START) row */
+  int32_t gh, gw;       /* patch grid of the image */
+  int64_t embed_row;    /* row of the image's first merged token in `embeds` */
+} ds_vit_span;
+
+/* Human-readable text of a return code (static storage). */
+const char* ds_vit_strerror(int code);
+
+/*
+ * ds_vit_prepare: validate `cfg`, keep the weight pointers (they must stay
+ * valid until ds_vit_release), allocate the device copies the kernels need
+ * (patch weight padded from K=588 to K=640 with zero columns, [A] Step 5; the
+ * first merger weight with its input permuted from c*9+p to p*1024+c; the RoPE
+ * cos/sin table; a device status word) and build the TMA descriptors.
+ * Synchronises `stream` before returning.  On error *out is NULL.
+ */
+int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w,
+                   ds_vit_prepared** out, void* stream);
+
+/* Free what ds_vit_prepare allocated (device-synchronising).  NULL is a no-op. */
+int ds_vit_release(ds_vit_prepared* p);
+
+/*
+ * ds_vit_layout (host only, no GPU needed): the token span of one image with a
+ * gh x gw patch grid ([A] "Connect the complete image-to-text path first";
+ * [B] V4.1 paragraph).  h = ceil(gh/3), w = ceil(gw/3); n = 2 + h*(w+1) rows:
+ * row 0 START; row 1 + y*(w+1) + x IMAGE with src = y*w + x; row
+ * 1 + y*(w+1) + w NEWLINE; row n-1 END.  ids[r] = image_token_id for every
+ * row, pos[r] = base_pos + r, src[r] = -1 for non-IMAGE rows.  Output arrays
+ * (host) need `cap` entries; *n_rows receives n (also when cap is too small,
+ * which returns DS_VIT_ECAP).  Any output pointer may be NULL to skip it.
+ */
+int ds_vit_layout(int32_t gh, int32_t gw, int32_t image_token_id, int32_t base_pos,
+                  int32_t* ids, int32_t* pos, uint8_t* type, int32_t* src,
+                  int64_t cap, int64_t* n_rows);
+
+/* Workspace bytes that ds_vit_encode_batch needs for these image sizes (host
+ * arrays of n entries).  Writes *bytes. */
+int ds_vit_workspace_bytes(const ds_vit_prepared* p, int n, const int32_t* H,
+                           const int32_t* W, size_t* bytes);
+
+/*
+ * ds_vit_encode_batch: encode n images (n <= DS_VIT_MAX_IMAGES) packed into one
+ * varlen pass; attention never crosses images.
+ *   pixels: host array of n device pointers, image i is uint8 [H[i], W[i], 3]
+ *           (HWC, RGB).  H[i], W[i] (host) must be positive multiples of 14;
+ *           (H/14)*(W/14) <= DS_VIT_MAX_PATCHES and the merged token count
+ *           ceil(H/42)*ceil(W/42) <= DS_VIT_MAX_TOKENS.
+ *   out:    device bf16 [sum T_i, 5120], image i's tokens at rows
+ *           tok_offsets[i] .. tok_offsets[i+1]-1 (row-major merged order).
+ *   tok_offsets: host int64 [n+1], written before the first launch.
+ *   ws, ws_bytes: device workspace of at least ds_vit_workspace_bytes.
+ */
+int ds_vit_encode_batch(const ds_vit_prepared* p, int n, const uint8_t* const* pixels,
+                        const int32_t* H, const int32_t* W, void* out, int64_t* tok_offsets,
+                        void* ws, size_t ws_bytes, void* stream);
+
+/* ds_vit_encode: one image (ds_vit_encode_batch with n = 1). */
+int ds_vit_encode(const ds_vit_prepared* p, const uint8_t* pixels, int32_t H, int32_t W,
+                  void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ds_vit_encode_batch_host: as ds_vit_encode_batch, but `pixels` holds HOST
+ * pointers and `out_host` is host memory.  The pixels are copied into the
+ * workspace (so ws_bytes must also cover sum H*W*3 rounded up, see
+ * ds_vit_workspace_bytes_host), the encode runs, and the result is copied to
+ * out_host; all on `stream`.  For full overlap the host buffers should be
+ * pinned.  The call returns after queueing; synchronise `stream` before reading
+ * out_host.
+ */
+int ds_vit_workspace_bytes_host(const ds_vit_prepared* p, int n, const int32_t* H,
+                                const int32_t* W, size_t* bytes);
+int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* const* pixels,
+                             const int32_t* H, const int32_t* W, void* out_host,
+                             int64_t* tok_offsets, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * ds_vit_encode_debug: ds_vit_encode_batch that also copies named boundaries
+ * ([A] Step 2: block outputs, final norm output) into caller buffers:
+ *   blocks: device bf16 [n_layers + 1, sum N_i, 1024] — the patch-projection
+ *           output followed by each block's output (NULL to skip);
+ *   final_norm: device bf16 [sum N_i, 1024] (NULL to skip).
+ */
+int ds_vit_encode_debug(const ds_vit_prepared* p, int n, const uint8_t* const* pixels,
+                        const int32_t* H, const int32_t* W, void* out, int64_t* tok_offsets,
+                        void* ws, size_t ws_bytes, void* blocks, void* final_norm,
+                        void* stream);
+
+/*
+ * ds_vit_overlay: write image spans into a prompt's hidden states
+ * ([A] "Connect the complete image-to-text path first": aligner rows replace
+ * IMAGE rows, learned vectors fill START / NEWLINE / END rows).  For span s
+ * and its row r (layout of ds_vit_layout for gh, gw):
+ *   hidden[base_row + r] = IMAGE ? embeds[embed_row + src] : sentinel[START/NEWLINE/END].
+ *   hidden:   device bf16 [n_hidden, width]; width = 5120.
+ *   spans:    host array of n_spans entries (n_spans <= DS_VIT_MAX_IMAGES);
+ *             every span must lie inside [0, n_hidden) and its embed rows
+ *             inside [0, n_embeds); spans must not overlap.
+ *   embeds:   device bf16 [n_embeds, width]; sentinel: device bf16 [3, width].
+ * Exact copy (bit-for-bit); rows outside the spans are not touched.
+ */
+int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_span* spans,
+                   int n_spans, const void* embeds, int64_t n_embeds, const void* sentinel,
+                   void* stream);
+
+/* Kernel kinds reported by ds_vit_set_kernel_timer. */
+#define DS_VIT_KERNEL_IM2COL 0
+#define DS_VIT_KERNEL_PATCH_GEMM 1
+#define DS_VIT_KERNEL_LAYERNORM 2
+#define DS_VIT_KERNEL_QKV_GEMM 3
+#define DS_VIT_KERNEL_ATTENTION 4
+#define DS_VIT_KERNEL_PROJ_GEMM 5
+#define DS_VIT_KERNEL_FC1_GEMM 6
+#define DS_VIT_KERNEL_FC2_GEMM 7
+#define DS_VIT_KERNEL_MERGE_GATHER 8
+#define DS_VIT_KERNEL_MERGER_GEMM1 9
+#define DS_VIT_KERNEL_MERGER_GEMM2 10
+
+/*
+ * ds_vit_set_kernel_timer (profiling aid): after this call, every kernel that
+ * an encode call on `p` launches is bracketed on its stream by
+ * cudaEventRecord(events[2i]) and cudaEventRecord(events[2i+1]) for the i-th
+ * launch of that call; kinds[i] receives its DS_VIT_KERNEL_* code and
+ * *n_recorded the number of launches of the latest call (launches past n_slots
+ * run untimed).  events: host array of 2*n_slots cudaEvent_t (created by the
+ * caller with timing enabled); kinds: host int32 [n_slots]; n_recorded: host
+ * int32.  All stay caller-owned and must outlive the attachment.
+ * events = NULL detaches.  Encodes on `p` must not run concurrently while
+ * attached.
+ */
+int ds_vit_set_kernel_timer(ds_vit_prepared* p, void* const* events, int32_t* kinds,
+                            int32_t n_slots, int32_t* n_recorded);
+
+/* Synchronise `stream`, then read and clear p's device status word: DS_VIT_OK,
+ * or DS_VIT_ETIMEOUT if a kernel's bounded wait gave up since the last read. */
+int ds_vit_device_status(const ds_vit_prepared* p, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Single-kernel entry points (the steps of the encode, for step-level parity
+ * checks and profiling).  `status` is a caller-owned device int32 that kernels
+ * with bounded waits set to DS_VIT_ETIMEOUT on a timeout (never cleared here).
+ * ------------------------------------------------------------------------- */
+
+/* y = bf16(LN(x) * g + b) over rows of 1024 (biased variance, fp32 statistics).
+ * x, y: device bf16 [M, 1024] (may not alias); g, b: device bf16 [1024]. */
+int ds_vit_op_layernorm(const void* x, const void* g, const void* b, void* y, int64_t M,
+                        float eps, void* stream);
+
+/* out[M, N] = epilogue(a[M, K] w[N, K]^T + bias[N]) on the tcgen05 tensor cores.
+ * K % 64 == 0, N % 256 == 0, M >= 1.  For DS_VIT_EPI_QKV_ROPE: N = 3072,
+ * rowpos (device int32 [M]) holds gy << 16 | gx of each row and rope_cs is the
+ * table of ds_vit_op_rope_table; otherwise both may be NULL. */
+int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t N,
+                     const void* bias, void* out, int32_t epilogue, const int32_t* rowpos,
+                     const float* rope_cs, int32_t* status, void* stream);
+
+/* rope_cs (device fp32 [max_pos, 32]): for pos < max_pos and i < 16,
+ * [pos][i] = cos(pos * theta^(-i/16)), [pos][16 + i] = sin(...), evaluated in
+ * double precision and rounded to fp32 ([A] Step 3). */
+int ds_vit_op_rope_table(float* rope_cs, int32_t max_pos, float theta, void* stream);
+
+/* Bidirectional attention per image over packed rows ([A] "Multimodal basics").
+ * qkv: device bf16 [total, 3072] (q | k | v, head h at columns h*64 of each);
+ * seqlens: host int32 [n_images]; out: device bf16 [total, 1024] =
+ * bf16(softmax(q k^T / 8) v) per image and head. */
+int ds_vit_op_attention(const void* qkv, const int32_t* seqlens, int n_images, void* out,
+                        int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSVIT_H */

@@ -5,6 +5,7 @@ leg may import it; the product path never does.  See ``oracle/encode.py``.
 """
 from .encode import (TOK_END, TOK_IMAGE, TOK_NEWLINE, TOK_START, attention, bits_to_f32,
                      block_tail, encode, f32_to_bits, gelu, grid_positions, layer_norm,
-                     layout, merge_unfold, merger, normalise, overlay, patchify, qkv_project,
+                     layout, merge_unfold, merger, mm, normalise, overlay, patchify, products,
+                     qkv_project,
                      rope, rope_angles, rope_freqs, round_bf16, softmax_rows, unpatchify,
                      vit_block)

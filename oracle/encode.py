@@ -45,6 +45,37 @@ F32 = np.float32
 TOK_START, TOK_IMAGE, TOK_NEWLINE, TOK_END = 0, 1, 2, 3
 
 
+# Matrix products.  Every product of the encode goes through ``mm``: an fp32
+# matrix product (BLAS sgemm; summation order is the library's).  With
+# ``products("f64")`` each dot product is accumulated in float64 and rounded to
+# fp32 once (the correctly rounded fp32 result in practice).  The two modes are
+# two valid evaluations of the same fp32 definition; tests use their difference
+# to measure how strongly the bf16 boundaries amplify summation-order noise.
+_PRODUCTS = ["f32"]
+
+
+def mm(a, b) -> np.ndarray:
+    if _PRODUCTS[0] == "f64":
+        return (np.asarray(a, np.float64) @ np.asarray(b, np.float64)).astype(F32)
+    return np.asarray(a, F32) @ np.asarray(b, F32)
+
+
+class products:
+    """Context manager selecting the accumulation of ``mm``: "f32" or "f64"."""
+
+    def __init__(self, mode: str):
+        assert mode in ("f32", "f64")
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = _PRODUCTS[0]
+        _PRODUCTS[0] = self.mode
+        return self
+
+    def __exit__(self, *exc):
+        _PRODUCTS[0] = self.prev
+
+
 def round_bf16(x) -> np.ndarray:
     """fp32 -> nearest bf16 value (ties to even), returned as fp32.
 
@@ -190,9 +221,9 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, heads: int,
     out = np.empty((q.shape[0], heads * head_dim), dtype=F32)
     for h in range(heads):
         sl = slice(h * head_dim, (h + 1) * head_dim)
-        s = (q[:, sl] @ k[:, sl].T) * scale
+        s = mm(q[:, sl], k[:, sl].T) * scale
         p = softmax_rows(s)
-        out[:, sl] = p @ v[:, sl]
+        out[:, sl] = mm(p, v[:, sl])
     return round_bf16(out)
 
 
@@ -207,7 +238,7 @@ def qkv_project(y, L, cfg, gy, gx):
     Page A, "Step 2" table (block 0 output isolates QKV bias, attention and
     residual order); page B's table: no QK norm."""
     D = cfg["hidden"]
-    t = y @ _f(L["qkv_w"]).T + _f(L["qkv_b"])
+    t = mm(y, _f(L["qkv_w"]).T) + _f(L["qkv_b"])
     q = round_bf16(rope(t[:, :D], gy, gx, cfg["rope_theta"]))
     k = round_bf16(rope(t[:, D:2 * D], gy, gx, cfg["rope_theta"]))
     v = round_bf16(t[:, 2 * D:])
@@ -218,10 +249,10 @@ def block_tail(x_rows, o_rows, L, cfg):
     """x = r(x + (o W_o^T + b_o)); y = r(LN2(x)); g = r(GELU(y W_1^T + b_1));
     x = r(x + (g W_2^T + b_2)).  Every stored activation is bf16 (page B)."""
     eps = cfg["ln_eps"]
-    x = round_bf16(x_rows + (o_rows @ _f(L["proj_w"]).T + _f(L["proj_b"])))
+    x = round_bf16(x_rows + (mm(o_rows, _f(L["proj_w"]).T) + _f(L["proj_b"])))
     y = round_bf16(layer_norm(x, _f(L["ln2_g"]), _f(L["ln2_b"]), eps))
-    g = round_bf16(gelu(y @ _f(L["fc1_w"]).T + _f(L["fc1_b"])))
-    return round_bf16(x + (g @ _f(L["fc2_w"]).T + _f(L["fc2_b"])))
+    g = round_bf16(gelu(mm(y, _f(L["fc1_w"]).T) + _f(L["fc1_b"])))
+    return round_bf16(x + (mm(g, _f(L["fc2_w"]).T) + _f(L["fc2_b"])))
 
 
 def vit_block(x, L, cfg, seqlens, gy, gx, rows=None):
@@ -269,8 +300,8 @@ def merge_unfold(z: np.ndarray, gh: int, gw: int, m: int = 3) -> np.ndarray:
 def merger(A: np.ndarray, W: dict) -> np.ndarray:
     """e = r(r(GELU(A W_m1^T + b_m1)) W_m2^T + b_m2) (page A, "Multimodal basics",
     third step, and "Step 2" table: the aligner's two linear projections)."""
-    u = round_bf16(gelu(A @ _f(W["m1_w"]).T + _f(W["m1_b"])))
-    return round_bf16(u @ _f(W["m2_w"]).T + _f(W["m2_b"]))
+    u = round_bf16(gelu(mm(A, _f(W["m1_w"]).T) + _f(W["m1_b"])))
+    return round_bf16(mm(u, _f(W["m2_w"]).T) + _f(W["m2_b"]))
 
 
 # ---------------------------------------------------------------- encode
@@ -297,7 +328,7 @@ def encode(images, W: dict, cfg: dict, n_layers: int | None = None, dump: dict |
     gy = np.concatenate([grid_positions(*g)[0] for g in grids])
     gx = np.concatenate([grid_positions(*g)[1] for g in grids])
     seqlens = [gh * gw for gh, gw in grids]
-    x = round_bf16(P @ _f(W["patch_w"]).T + _f(W["patch_b"]))
+    x = round_bf16(mm(P, _f(W["patch_w"]).T) + _f(W["patch_b"]))
     if dump is not None:
         dump["patches"], dump["x0"], dump["blocks"] = P, x, []
     for L in L_all:

@@ -1,0 +1,95 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol the header
+declares, validates arguments before touching CUDA, and its host-only layout
+matches the oracle exactly."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import vit_vision_encoder_gb300
+    return vit_vision_encoder_gb300
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsvit.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ds_vit_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(dv):
+    names = _declared()
+    assert len(names) >= 15
+    h = C.CDLL(dv.LIB_PATH)
+    for n in names:
+        assert hasattr(h, n), n
+    assert set(names) == set(dv.SIGNATURES)
+
+
+def test_strerror(dv):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert dv.lib.ds_vit_strerror(code)
+    assert dv.lib.ds_vit_strerror(-99) == b"unknown error"
+
+
+@pytest.mark.parametrize("H,W", [(84, 84), (546, 546), (1344, 1344), (2688, 336), (1344, 672),
+                                 (672, 1344), (1008, 1008), (840, 420), (14, 14), (14, 9 * 14 * 14),
+                                 (70, 28)])
+def test_layout_matches_oracle(dv, H, W):
+    gh, gw = H // 14, W // 14
+    got = dv.layout(gh, gw, 129264, base_pos=1000)
+    ref = O.layout(gh, gw, 129264, base_pos=1000)
+    for g, r in zip(got, ref):
+        assert np.array_equal(g, r)
+
+
+def test_layout_capacity_and_args(dv):
+    n = C.c_int64(0)
+    ids = np.zeros(3, np.int32)
+    assert dv.lib.ds_vit_layout(6, 6, 1, 0, ids.ctypes.data, None, None, None, 3, C.byref(n)) == dv.ECAP
+    assert n.value == 8 and np.all(ids == 0)          # nothing written on error
+    assert dv.lib.ds_vit_layout(0, 6, 1, 0, None, None, None, None, 0, C.byref(n)) == dv.EINVAL
+    assert dv.lib.ds_vit_layout(6, 6, 1, 2 ** 31 - 5, None, None, None, None, 100, C.byref(n)) == dv.ERANGE
+
+
+def test_null_arguments_rejected_before_cuda(dv):
+    L = dv.lib
+    assert L.ds_vit_prepare(None, None, None, None) == dv.EINVAL
+    h = C.c_void_p()
+    cfg = dv.make_config(WL.MODEL, 2)
+    assert L.ds_vit_prepare(C.byref(cfg), None, C.byref(h), None) == dv.EINVAL
+    bad = dv.make_config(dict(WL.MODEL, hidden=768), 2)
+    w = dv.Weights()
+    assert L.ds_vit_prepare(C.byref(bad), C.byref(w), C.byref(h), None) == dv.EINVAL
+    assert L.ds_vit_overlay(None, 10, 5120, None, 1, None, 1, None, None) == dv.EINVAL
+    assert L.ds_vit_encode(None, None, 84, 84, None, None, 0, None) == dv.EINVAL
+    assert L.ds_vit_release(None) == dv.OK
+    assert L.ds_vit_device_status(None, None) == dv.EINVAL
+    assert L.ds_vit_op_attention(None, None, 1, None, None, None) == dv.EINVAL
+    assert L.ds_vit_op_linear(None, 1, 64, None, 256, None, None, 0, None, None, None, None) == dv.EINVAL
+
+
+def test_workspace_size_validation(dv):
+    # a non-multiple of 14 and an image over the 9216-patch limit are refused
+    L = dv.lib
+    b = C.c_size_t(0)
+    fake = C.c_void_p(1)
+    H = (C.c_int32 * 1)(85)
+    W = (C.c_int32 * 1)(84)
+    assert L.ds_vit_workspace_bytes(fake, 1, H, W, C.byref(b)) == dv.EINVAL
+    H[0], W[0] = 1358, 1344        # 97 x 96 patches
+    assert L.ds_vit_workspace_bytes(fake, 1, H, W, C.byref(b)) == dv.ERANGE
+    H[0], W[0] = 1344, 1344
+    assert L.ds_vit_workspace_bytes(fake, 1, H, W, C.byref(b)) == dv.OK
+    assert b.value >= 9216 * (1024 * 3 + 3072 + 4096) * 2

@@ -1,0 +1,357 @@
+// tcgen05 GEMM for the encode's dense contractions: out = epi(A B^T + bias).
+//
+// A [M, K] (activations) and B [N, K] (nn.Linear weights) are both K-major
+// bf16, staged by TMA into 128-byte-swizzled shared-memory tiles; one thread
+// issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM
+// accumulator; four epilogue warps read it back with tcgen05.ld and apply the
+// fused epilogue:
+//   bias                 — patch projection ("Multimodal basics": a patch
+//                          projection maps pixel rows into the vision hidden
+//                          space) and the second merger linear;
+//   bias + GELU(erf)     — MLP up-projection and the first merger linear
+//                          ("End-to-end results and their limits": erf GELU);
+//   bias + residual      — attention output projection and MLP down-projection
+//                          (pre-norm block, residual stream stored in bf16);
+//   bias + 2D RoPE       — QKV projection: q and k rotated per head, dims 0..31
+//                          by the patch row and 32..63 by the patch column with
+//                          the half-vector pairing (j, j+16) ("Step 3: Height and
+//                          width occupy blocks in 2D RoPE").
+// All from "DeepSeek V4.1 Flash Engineering, Part 3: Integrating Vision".
+//
+// Structure: persistent CTAs (one per SM), 6 warps: warps 0-3 epilogue (TMEM
+// lane quadrant = warp index), warp 4 TMA producer, warp 5 MMA issuer.  A ring
+// of STAGES shared-memory stages (full/empty mbarriers) feeds the MMA; two TMEM
+// accumulators (tfull/tempty mbarriers) let the epilogue of one tile overlap
+// the main loop of the next.
+#include "internal.h"
+#include "ptx.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace dsvit {
+
+namespace {
+
+struct GemmParams {
+  int M, N, K;
+  bf16* out;
+  const bf16* bias;
+  const int* rowpos;
+  const float* rope_cs;
+  int* status;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int BK = 64;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+};
+
+__device__ __forceinline__ float gelu_erf(float x) {
+  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+  auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
+  auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  auto stage_a = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
+  auto stage_b = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int num_m = (p.M + C::BM - 1) / C::BM;
+  const int num_n = p.N / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = p.K / C::BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull_bar(a), 1);
+      mbar_init(tempty_bar(a), 4);
+    }
+    mbar_init(drain_bar, 1);
+    fence_barrier_init();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  __shared__ int consumed_fills;
+  int issued_fills = 0;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const int mb = tile % num_m, nb = tile / num_m;
+        bool ok = true;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * C::BK, mb * C::BM);
+          tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
+          ++issued_fills;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false, false);
+      int stage = 0, fills = 0;
+      uint32_t phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), acc_phase ^ 1u, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(full_bar(stage), phase, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
+#pragma unroll
+          for (int k = 0; k < C::BK / 16; ++k) {
+            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
+                      idesc, (kb | k) != 0);
+          }
+          umma_commit(empty_bar(stage));
+          ++fills;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(tfull_bar(acc));
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      consumed_fills = fills;
+      // All MMAs of this CTA complete before TMEM is released.
+      umma_commit(drain_bar);
+      mbar_wait(drain_bar, 0, p.status);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-3)
+    uint32_t acc = 0, acc_phase = 0;
+    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const int mb = tile % num_m, nb = tile / num_m;
+      if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
+      tc_fence_after();
+      const int row = mb * C::BM + warp * 32 + lane;
+      const bool valid = row < p.M;
+      int gy = 0, gx = 0;
+      if constexpr (EPI == kEpiQkvRope) {
+        if (valid) {
+          const int rp = __ldg(p.rowpos + row);
+          gy = rp >> 16;
+          gx = rp & 0xFFFF;
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem_base + acc * BN + c * 32 + lane_sel, r);
+        tmem_wait_ld();
+        if (c == BN / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(acc));
+        }
+        const int n0 = nb * BN + c * 32;
+        float v[32];
+        const uint4* bias4 = reinterpret_cast<const uint4*>(p.bias + n0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 b = __ldg(bias4 + q);
+          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            v[q * 8 + 2 * e] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e]), bf16lo(bw[e]));
+            v[q * 8 + 2 * e + 1] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e + 1]), bf16hi(bw[e]));
+          }
+        }
+        bf16* dst = p.out + static_cast<size_t>(row) * p.N + n0;
+        if constexpr (EPI == kEpiBiasGelu) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+        } else if constexpr (EPI == kEpiBiasResid) {
+          if (valid) {
+            const uint4* src = reinterpret_cast<const uint4*>(dst);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 x = src[q];
+              const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                v[q * 8 + 2 * e] = __fadd_rn(bf16lo(xw[e]), v[q * 8 + 2 * e]);
+                v[q * 8 + 2 * e + 1] = __fadd_rn(bf16hi(xw[e]), v[q * 8 + 2 * e + 1]);
+              }
+            }
+          }
+        } else if constexpr (EPI == kEpiQkvRope) {
+          if (n0 < 2048) {
+            // 32 columns = one rotary half of one head: dims 0..31 -> row, 32..63 -> column.
+            const int pos = ((n0 >> 5) & 1) ? gx : gy;
+            const float* cs = p.rope_cs + pos * 32;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float cj = __ldg(cs + j), sj = __ldg(cs + 16 + j);
+              const float a = v[j], b = v[j + 16];
+              v[j] = __fsub_rn(__fmul_rn(a, cj), __fmul_rn(b, sj));
+              v[j + 16] = __fadd_rn(__fmul_rn(b, cj), __fmul_rn(a, sj));
+            }
+          }
+        }
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
+                               pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
+                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
+                               pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
+          }
+        }
+      }
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4 && lane == 0 && status_failed(p.status)) {
+    // After a timeout: wait (bounded) for the tile loads still in flight, so no
+    // TMA write lands in shared memory after the CTA has exited.
+    for (int f = consumed_fills; f < issued_fills; ++f) {
+      const int s = f % C::STAGES;
+      if (!mbar_wait(full_bar(s), (f / C::STAGES) & 1, nullptr)) break;
+    }
+  }
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, int EPI>
+int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                  cudaStream_t stream) {
+  using C = GemmCfg<BN>;
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
+  const int tiles = ((p.M + 127) / 128) * (p.N / BN);
+  const int grid = tiles < num_sms() ? tiles : num_sms();
+  gemm_kernel<BN, EPI><<<grid, 192, C::SMEM_BYTES, stream>>>(tmA, tmB, p);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!encode || !base || rows == 0 || cols == 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_bn(int /*M*/, int /*N*/) { return 256; }
+
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                const bf16* bias, bf16* out, int epi, const int* rowpos, const float* rope_cs,
+                int* status, cudaStream_t stream) {
+  if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
+  GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status};
+  switch (epi) {
+    case kEpiBias: return launch_gemm_t<256, kEpiBias>(tmA, tmB, p, stream);
+    case kEpiBiasGelu: return launch_gemm_t<256, kEpiBiasGelu>(tmA, tmB, p, stream);
+    case kEpiBiasResid: return launch_gemm_t<256, kEpiBiasResid>(tmA, tmB, p, stream);
+    case kEpiQkvRope: return launch_gemm_t<256, kEpiQkvRope>(tmA, tmB, p, stream);
+    default: return DS_VIT_EINVAL;
+  }
+}
+
+}  // namespace dsvit

@@ -1,0 +1,91 @@
+// Declarations shared by the translation units of libdsvit (not part of the ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsvit.h"
+
+namespace dsvit {
+
+using bf16 = __nv_bfloat16;
+
+// Epilogue kinds of the tcgen05 GEMM (same values as DS_VIT_EPI_*).
+enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3 };
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point.
+// Row-major bf16 matrix [rows, cols], box [box_rows, 64 cols], 128-byte swizzle,
+// zero fill out of bounds.  Returns false on failure.
+bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                    uint32_t box_rows);
+
+int num_sms();
+
+// out[M, N] = epi(A[M, K] B[N, K]^T + bias); tmB describes B with box rows == BN.
+// Returns DS_VIT_OK or DS_VIT_ECUDA.
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
+                const bf16* bias, bf16* out, int epi, const int* rowpos, const float* rope_cs,
+                int* status, cudaStream_t stream);
+
+// The BN that launch_gemm uses for an N-wide output (the B tensor map's box rows).
+int gemm_bn(int M, int N);
+
+struct AttnBatch {
+  int n_images;
+  int cu[DS_VIT_MAX_IMAGES + 1];          // packed row offsets of the images
+  int tile_start[DS_VIT_MAX_IMAGES + 1];  // q-tile prefix sums in launch order
+  int order[DS_VIT_MAX_IMAGES];           // launch slot -> image index
+};
+
+int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* out, int* status,
+                     cudaStream_t stream);
+
+int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
+                     cudaStream_t stream);
+
+struct ImageBatch {
+  int n;
+  int64_t row_off[DS_VIT_MAX_IMAGES + 1];  // patch row offsets
+  int64_t tok_off[DS_VIT_MAX_IMAGES + 1];  // merged token offsets
+  const uint8_t* pix[DS_VIT_MAX_IMAGES];
+  int gh[DS_VIT_MAX_IMAGES];
+  int gw[DS_VIT_MAX_IMAGES];
+};
+
+struct PixelNorm {
+  float mean[3];
+  float std[3];
+};
+
+// Patchify + normalise into A_pe [sum N, 640] (columns 588..639 zero) and the
+// per-row position word gy << 16 | gx.
+int launch_im2col(const ImageBatch& batch, const PixelNorm& norm, bf16* a_pe, int* rowpos,
+                  cudaStream_t stream);
+
+// Gather z [sum N, 1024] into the merger input [sum T, 9216] with column
+// p*1024 + c (p = dy*3 + dx), zero where the 3x3 window leaves the grid.
+int launch_merge_gather(const ImageBatch& batch, const bf16* z, bf16* a_m, cudaStream_t stream);
+
+int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream);
+
+// W'[o, p*1024 + c] = W[o, c*9 + p]  (rows of 9216).
+int launch_permute_m1(const bf16* w, bf16* w_perm, int rows, cudaStream_t stream);
+
+// W'[o, k] = k < 588 ? W[o, k] : 0  (rows of 640).
+int launch_pad_patch_w(const bf16* w, bf16* w_pad, int rows, cudaStream_t stream);
+
+struct OverlaySpans {
+  int n;
+  int64_t base_row[DS_VIT_MAX_IMAGES];
+  int64_t embed_row[DS_VIT_MAX_IMAGES];
+  int h[DS_VIT_MAX_IMAGES];   // merged grid
+  int w[DS_VIT_MAX_IMAGES];
+  int64_t row_start[DS_VIT_MAX_IMAGES + 1];  // prefix of span row counts
+};
+
+int launch_overlay(bf16* hidden, int width, const OverlaySpans& spans, const bf16* embeds,
+                   const bf16* sentinel, cudaStream_t stream);
+
+}  // namespace dsvit

@@ -1,0 +1,244 @@
+// Memory-bound kernels of the encode: LayerNorm, patchify + normalise
+// (im2col), the 3x3 merge-gather, the RoPE table, weight preparation and the
+// overlay scatter.  Sources: "DeepSeek V4.1 Flash Engineering, Part 3:
+// Integrating Vision" (cited per kernel).
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace dsvit {
+
+namespace {
+
+// ---------------------------------------------------------------- LayerNorm
+// One warp per 1024-wide row; each lane holds 32 values (four 16-byte loads,
+// coalesced across the warp).  fp32 statistics: mean, then the biased variance
+// of the centred values; y = (x - mu) * (1/sqrt(var + eps)) * g + b rounded to
+// bf16 ("Step 2": the final-norm boundary; block pre-norms).
+__global__ void __launch_bounds__(256) layernorm_kernel(const bf16* __restrict__ x,
+                                                        const bf16* __restrict__ g,
+                                                        const bf16* __restrict__ b,
+                                                        bf16* __restrict__ y, int64_t M,
+                                                        float eps) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  if (row >= M) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * 1024);
+  float v[32];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 u = xr[q * 32 + lane];
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[q * 8 + 2 * e] = bf16lo(w[e]);
+      v[q * 8 + 2 * e + 1] = bf16hi(w[e]);
+    }
+  }
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) s += v[i];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+  const float mu = __fdiv_rn(s, 1024.f);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    v[i] = __fsub_rn(v[i], mu);
+    ss = __fmaf_rn(v[i], v[i], ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+  const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1024.f), eps)));
+  const uint4* g4 = reinterpret_cast<const uint4*>(g);
+  const uint4* b4 = reinterpret_cast<const uint4*>(b);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * 1024);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 gu = __ldg(g4 + q * 32 + lane), bu = __ldg(b4 + q * 32 + lane);
+    const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w}, bw[4] = {bu.x, bu.y, bu.z, bu.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float y0 = __fadd_rn(__fmul_rn(__fmul_rn(v[q * 8 + 2 * e], inv), bf16lo(gw[e])), bf16lo(bw[e]));
+      const float y1 =
+          __fadd_rn(__fmul_rn(__fmul_rn(v[q * 8 + 2 * e + 1], inv), bf16hi(gw[e])), bf16hi(bw[e]));
+      o[e] = pack_bf16x2(y0, y1);
+    }
+    yr[q * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// ---------------------------------------------------------------- patchify
+// Row n of image i = patch (gy, gx) = (n / gw, n % gw); column k = c*196 +
+// y*14 + x holds pixel (gy*14 + y, gx*14 + x, c) mapped to
+// bf16((p/255 - mean_c)/std_c) ("Step 1", items 5 and 6; "Step 5": 588
+// columns, here padded with zeros to 640 for 64-wide K tiles).
+// One block of 160 threads per patch row; thread t writes 4 columns.
+__global__ void __launch_bounds__(160) im2col_kernel(const __grid_constant__ ImageBatch batch,
+                                                     const __grid_constant__ PixelNorm norm,
+                                                     bf16* __restrict__ a_pe, int* __restrict__ rowpos) {
+  const int64_t n = blockIdx.x;
+  int i = 0;
+  while (i + 1 < batch.n && batch.row_off[i + 1] <= n) ++i;
+  const int local = static_cast<int>(n - batch.row_off[i]);
+  const int gw = batch.gw[i];
+  const int gy = local / gw, gx = local % gw;
+  const int W = gw * 14;
+  const uint8_t* pix = batch.pix[i];
+  if (threadIdx.x == 0) rowpos[n] = (gy << 16) | gx;
+  uint32_t out[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float f[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int k = threadIdx.x * 4 + h * 2 + e;
+      float val = 0.f;
+      if (k < 588) {
+        const int c = k / 196, rem = k % 196, y = rem / 14, x = rem % 14;
+        const float p = static_cast<float>(pix[(static_cast<int64_t>(gy * 14 + y) * W + gx * 14 + x) * 3 + c]);
+        val = __fdiv_rn(__fsub_rn(__fdiv_rn(p, 255.f), norm.mean[c]), norm.std[c]);
+      }
+      f[e] = val;
+    }
+    out[h] = pack_bf16x2(f[0], f[1]);
+  }
+  *reinterpret_cast<uint2*>(a_pe + n * 640 + threadIdx.x * 4) = make_uint2(out[0], out[1]);
+}
+
+// ---------------------------------------------------------------- merge-gather
+// Merged token t = my*w + mx of image i, window position p = dy*3 + dx:
+// A[t, p*1024 + c] = z[(3my+dy)*gw + 3mx+dx, c], or 0 when (3my+dy, 3mx+dx)
+// falls in the right/bottom padding ("Step 4: The aligner pads a
+// two-dimensional grid").  The position-major column order matches the
+// merger weight permuted at preparation (same sum as the channel-major unfold).
+// Block = one merged token, 9 x 128 threads of 16 bytes.
+__global__ void __launch_bounds__(128) merge_gather_kernel(const __grid_constant__ ImageBatch batch,
+                                                           const bf16* __restrict__ z,
+                                                           bf16* __restrict__ a_m) {
+  const int64_t t = blockIdx.x;
+  int i = 0;
+  while (i + 1 < batch.n && batch.tok_off[i + 1] <= t) ++i;
+  const int local = static_cast<int>(t - batch.tok_off[i]);
+  const int gh = batch.gh[i], gw = batch.gw[i];
+  const int w = (gw + 2) / 3;
+  const int my = local / w, mx = local % w;
+  uint4* dst = reinterpret_cast<uint4*>(a_m + t * 9216);
+#pragma unroll
+  for (int p = 0; p < 9; ++p) {
+    const int sy = 3 * my + p / 3, sx = 3 * mx + p % 3;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (sy < gh && sx < gw) {
+      const uint4* src = reinterpret_cast<const uint4*>(z + (batch.row_off[i] + sy * gw + sx) * 1024);
+      v = src[threadIdx.x];
+    }
+    dst[p * 128 + threadIdx.x] = v;
+  }
+}
+
+// ---------------------------------------------------------------- RoPE table
+// [pos][i] = cos(pos * theta^(-i/16)), [pos][16+i] = sin(...), in double, cast
+// to fp32 ("Step 3": height and width frequencies, 16 per 32-dim half).
+__global__ void rope_table_kernel(float* table, int max_pos, double theta) {
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= max_pos * 16) return;
+  const int pos = idx / 16, i = idx % 16;
+  const double f = pow(theta, -static_cast<double>(i) / 16.0);
+  const double a = static_cast<double>(pos) * f;
+  table[pos * 32 + i] = static_cast<float>(cos(a));
+  table[pos * 32 + 16 + i] = static_cast<float>(sin(a));
+}
+
+__global__ void permute_m1_kernel(const bf16* __restrict__ w, bf16* __restrict__ wp) {
+  const int64_t o = blockIdx.x;
+  for (int k = threadIdx.x; k < 9216; k += blockDim.x) {
+    const int p = k / 1024, c = k % 1024;
+    wp[o * 9216 + k] = w[o * 9216 + c * 9 + p];
+  }
+}
+
+__global__ void pad_patch_w_kernel(const bf16* __restrict__ w, bf16* __restrict__ wp) {
+  const int64_t o = blockIdx.x;
+  for (int k = threadIdx.x; k < 640; k += blockDim.x)
+    wp[o * 640 + k] = k < 588 ? w[o * 588 + k] : __float2bfloat16_rn(0.f);
+}
+
+// ---------------------------------------------------------------- overlay
+// Span row r of span s: r = 0 START, r = n-1 END, otherwise q = r-1,
+// y = q / (w+1), x = q % (w+1): NEWLINE when x == w, else IMAGE with merged
+// token y*w + x ("Connect the complete image-to-text path first").  IMAGE rows
+// copy the aligner row, the others the learned vector.  One block per row,
+// 16-byte vector copies.
+__global__ void __launch_bounds__(128) overlay_kernel(bf16* __restrict__ hidden, int width,
+                                                      const __grid_constant__ OverlaySpans spans,
+                                                      const bf16* __restrict__ embeds,
+                                                      const bf16* __restrict__ sentinel) {
+  const int64_t g = blockIdx.x;
+  int s = 0;
+  while (s + 1 < spans.n && spans.row_start[s + 1] <= g) ++s;
+  const int64_t r = g - spans.row_start[s];
+  const int64_t n = spans.row_start[s + 1] - spans.row_start[s];
+  const int w = spans.w[s];
+  const bf16* src;
+  if (r == 0) {
+    src = sentinel;
+  } else if (r == n - 1) {
+    src = sentinel + 2 * static_cast<int64_t>(width);
+  } else {
+    const int64_t q = r - 1, y = q / (w + 1), x = q % (w + 1);
+    src = (x == w) ? sentinel + width : embeds + (spans.embed_row[s] + y * w + x) * width;
+  }
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(hidden + (spans.base_row[s] + r) * width);
+  for (int k = threadIdx.x; k < width / 8; k += blockDim.x) d4[k] = s4[k];
+}
+
+}  // namespace
+
+int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
+                     cudaStream_t stream) {
+  if (M <= 0) return DS_VIT_OK;
+  layernorm_kernel<<<static_cast<unsigned>((M + 7) / 8), 256, 0, stream>>>(x, g, b, y, M, eps);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_im2col(const ImageBatch& batch, const PixelNorm& norm, bf16* a_pe, int* rowpos,
+                  cudaStream_t stream) {
+  const int64_t rows = batch.row_off[batch.n];
+  if (rows <= 0) return DS_VIT_OK;
+  im2col_kernel<<<static_cast<unsigned>(rows), 160, 0, stream>>>(batch, norm, a_pe, rowpos);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_merge_gather(const ImageBatch& batch, const bf16* z, bf16* a_m, cudaStream_t stream) {
+  const int64_t toks = batch.tok_off[batch.n];
+  if (toks <= 0) return DS_VIT_OK;
+  merge_gather_kernel<<<static_cast<unsigned>(toks), 128, 0, stream>>>(batch, z, a_m);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream) {
+  const int n = max_pos * 16;
+  rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(table, max_pos, static_cast<double>(theta));
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_permute_m1(const bf16* w, bf16* w_perm, int rows, cudaStream_t stream) {
+  permute_m1_kernel<<<rows, 256, 0, stream>>>(w, w_perm);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_pad_patch_w(const bf16* w, bf16* w_pad, int rows, cudaStream_t stream) {
+  pad_patch_w_kernel<<<rows, 128, 0, stream>>>(w, w_pad);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_overlay(bf16* hidden, int width, const OverlaySpans& spans, const bf16* embeds,
+                   const bf16* sentinel, cudaStream_t stream) {
+  const int64_t rows = spans.row_start[spans.n];
+  if (rows <= 0) return DS_VIT_OK;
+  overlay_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(hidden, width, spans, embeds, sentinel);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+}  // namespace dsvit

@@ -181,6 +181,28 @@ int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* con
                              int64_t* tok_offsets, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ds_vit_encode_noalloc: ds_vit_encode for callers that cannot allocate device
+ * memory when they encode (an application that owns the whole device budget
+ * through its own pool, a latency-critical loop that must not pay cudaMalloc's
+ * implicit synchronisation, a plugin interface that passes only inputs and
+ * outputs).  The pages have no counterpart: it is a deployment variant.
+ *   Same arguments and results as ds_vit_encode, without ws/ws_bytes: the
+ *   scratch is a file-scope device array of DS_VIT_NOALLOC_SCRATCH_BYTES
+ *   inside the library, held by every GPU that loads the library until exit.
+ *   Images over DS_VIT_NOALLOC_MAX_PATCHES patches return DS_VIT_ERANGE (after
+ *   the usual DS_VIT_EINVAL checks) and nothing is written.
+ *   The call allocates and frees nothing.  Its first call on a device looks up
+ *   the array's device address on that device (cudaGetSymbolAddress, with the
+ *   device current); make that first call before any stream capture.
+ *   All calls share the array and it keeps the last call's contents (no part
+ *   needs to start at zero); calls whose kernels overlap on the GPU race.
+ */
+#define DS_VIT_NOALLOC_MAX_PATCHES 1024                   /* e.g. 448 x 448 pixels */
+#define DS_VIT_NOALLOC_SCRATCH_BYTES (21u * 1024u * 1024u) /* 21 MiB */
+int ds_vit_encode_noalloc(const ds_vit_prepared* p, const uint8_t* pixels, int32_t H, int32_t W,
+                          void* out, void* stream);
+
+/*
  * ds_vit_encode_debug: ds_vit_encode_batch that also copies named boundaries
  * ([A] Step 2: block outputs, final norm output) into caller buffers:
  *   blocks: device bf16 [n_layers + 1, sum N_i, 1024] — the patch-projection

@@ -93,3 +93,18 @@ def test_workspace_size_validation(dv):
     H[0], W[0] = 1344, 1344
     assert L.ds_vit_workspace_bytes(fake, 1, H, W, C.byref(b)) == dv.OK
     assert b.value >= 9216 * (1024 * 3 + 3072 + 4096) * 2
+
+
+def test_no_alloc_scratch_covers_every_grid_up_to_the_limit(dv):
+    """Every grid of at most NOALLOC_MAX_PATCHES patches fits the static scratch."""
+    L = dv.lib
+    b = C.c_size_t(0)
+    fake = C.c_void_p(1)
+    worst = 0
+    for gh in range(1, dv.NOALLOC_MAX_PATCHES + 1):
+        for gw in (dv.NOALLOC_MAX_PATCHES // gh,):
+            H = (C.c_int32 * 1)(14 * gh)
+            W = (C.c_int32 * 1)(14 * gw)
+            assert L.ds_vit_workspace_bytes(fake, 1, H, W, C.byref(b)) == dv.OK
+            worst = max(worst, b.value)
+    assert worst <= dv.NOALLOC_SCRATCH_BYTES

@@ -19,6 +19,7 @@ OK, EINVAL, ERANGE, ECAP, ECUDA, ETIMEOUT, ENOMEM = 0, -1, -2, -3, -4, -5, -6
 TOK_START, TOK_IMAGE, TOK_NEWLINE, TOK_END = 0, 1, 2, 3
 EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESID, EPI_QKV_ROPE = 0, 1, 2, 3
 MAX_LAYERS, MAX_IMAGES, MAX_PATCHES, MAX_TOKENS = 32, 64, 9216, 1024
+NOALLOC_MAX_PATCHES, NOALLOC_SCRATCH_BYTES = 1024, 21 * 1024 * 1024
 
 
 class DsVitError(RuntimeError):
@@ -68,6 +69,7 @@ SIGNATURES = {
     "ds_vit_encode_batch": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,
                                       _VP, _SZ, _VP]),
     "ds_vit_encode": (C.c_int, [_VP, _VP, _I32, _I32, _VP, _VP, _SZ, _VP]),
+    "ds_vit_encode_noalloc": (C.c_int, [_VP, _VP, _I32, _I32, _VP, _VP]),
     "ds_vit_encode_batch_host": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP,
                                            _P_I64, _VP, _SZ, _VP]),
     "ds_vit_encode_debug": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,

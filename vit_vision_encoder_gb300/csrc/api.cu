@@ -162,7 +162,8 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
   });
   for (int k = 0; k < n; ++k) {
     const int i = ab.order[k];
-    ab.tile_start[k + 1] = ab.tile_start[k] + (ab.cu[i + 1] - ab.cu[i] + 127) / 128;
+    ab.tile_start[k + 1] =
+        ab.tile_start[k] + (ab.cu[i + 1] - ab.cu[i] + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
   }
   const int64_t N = pl.N, T = pl.T;
   bf16* x = reinterpret_cast<bf16*>(ws + pl.off_x);
@@ -538,7 +539,7 @@ int ds_vit_op_attention(const void* qkv, const int32_t* seqlens, int n_images, v
     if (seqlens[i] < 1 || seqlens[i] > DS_VIT_MAX_PATCHES) return DS_VIT_ERANGE;
     ab.cu[i + 1] = ab.cu[i] + seqlens[i];
     ab.order[i] = i;
-    ab.tile_start[i + 1] = ab.tile_start[i] + (seqlens[i] + 127) / 128;
+    ab.tile_start[i + 1] = ab.tile_start[i] + (seqlens[i] + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
   }
   CUtensorMap tm;
   if (!make_tmap_bf16(&tm, qkv, ab.cu[n_images], 3072, 128)) return DS_VIT_ECUDA;

@@ -7,16 +7,20 @@
 // Softmax scale 1/sqrt(64), no mask inside an image, no QK norm (ds4-learning
 // glossary "vision", family table).
 //
-// One CTA = one (image, 128-row query tile, head).  Warps 0-3 own one query
-// row per thread (TMEM lane = row); warp 4 loads Q once and streams K/V tiles
-// of 128 rows through a 3-stage TMA ring; warp 5 issues the MMAs:
-//   S_j = Q K_j^T          (M 128, N 128, K 64)  -> TMEM, double-buffered
-//   O  += P_j V_j          (M 128, N 64,  K 128) -> TMEM
-// The softmax warps read S_j from TMEM, keep the running row max m and sum l
-// in registers (exp2 domain), write P_j = exp2(s - m) as bf16 into a
-// 128-byte-swizzled shared tile (the MMA's A operand), and rescale O in TMEM
-// by exp2(m_old - m_new) when the max grows.  S_{j+1} is computed while the
-// softmax of tile j runs.  Final O / l is written as bf16.
+// One CTA = one (image, 256 query rows, head), as two 128-row query tiles A
+// and B that share every K/V tile.  Warps 0-3 run the softmax of tile A and
+// warps 4-7 that of tile B (one query row per thread, TMEM lane = row); warp 8
+// loads Q once and streams K/V tiles of 128 rows through a 3-stage TMA ring;
+// warp 9 issues the MMAs:
+//   S_X = Q_X K_j^T     (M 128, N 128, K 64)  -> TMEM, one buffer per tile X
+//   O_X += P_X V_j      (M 128, N 64,  K 128) -> TMEM
+// A softmax warpgroup reads S_X from TMEM and hands the buffer back at once,
+// so the next S_X is computed while it works; the two warpgroups alternate
+// on the tensor core.  The running row maximum m (exp2 domain) is raised only
+// when a tile's maximum exceeds it by more than 8, so P = exp2(s - m) stays
+// below 2^8 and O is rescaled (in TMEM, by exp2(m_old - m_new)) rarely; the
+// final O / l uses the same m, so the result is the exact softmax.  P is
+// written as bf16 into a 128-byte-swizzled shared tile, the PV MMA's A operand.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -26,20 +30,34 @@ namespace dsvit {
 
 namespace {
 
-constexpr int kTile = 128;     // query rows per CTA and key rows per K/V tile
+constexpr int kTile = 128;     // rows of a query tile and of a K/V tile
 constexpr int kHd = 64;        // head dim
 constexpr int kStages = 3;     // K/V ring depth
-constexpr int kQBytes = kTile * kHd * 2;              // 16 KB
+constexpr int kQBytes = kTile * kHd * 2;              // 16 KB per query tile
 constexpr int kKVBytes = kTile * kHd * 2;             // 16 KB each for K and V
 constexpr int kPBytes = kTile * kTile * 2;            // 32 KB (two 64-column chunks)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffQ = 0;                              // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kQBytes;
 constexpr int kOffV = kOffK + kStages * kKVBytes;
-constexpr int kOffP = kOffV + kStages * kKVBytes;
+constexpr int kOffP = kOffV + kStages * kKVBytes;     // P_A, P_B
 constexpr int kOffBar = kOffP + 2 * kPBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
-constexpr uint32_t kTmemCols = 512;   // S0 [0,128), S1 [128,256), O [256,320)
+constexpr uint32_t kTmemCols = 512;   // S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384)
 constexpr uint32_t kTmemO = 256;
+constexpr int kThreads = 320;         // 8 softmax warps, TMA warp, MMA warp
+constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays below 2^8
+
+// Barrier slots (8 bytes each).
+enum : int {
+  kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = kBarKvFull + kStages,
+  kBarSFull = kBarKvEmpty + kStages,   // [2]
+  kBarSFree = kBarSFull + 2,           // [2]
+  kBarPFull = kBarSFree + 2,           // [2]
+  kBarPvDone = kBarPFull + 2,          // [2]
+  kBarDrain = kBarPvDone + 2,
+  kBarCount = kBarDrain + 1
+};
+static_assert(kBarCount <= 30, "barrier area");
 
 struct AttnParams {
   AttnBatch b;
@@ -48,53 +66,72 @@ struct AttnParams {
   float scale_log2;  // log2(e) / sqrt(64)
 };
 
-__global__ void __launch_bounds__(192, 1)
+__device__ __forceinline__ uint64_t f2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 31);
   const uint32_t bar0 = smem_u32(bars);
-  const uint32_t q_full = bar0;
-  auto kv_full = [&](int s) { return bar0 + 8u * (1 + s); };
-  auto kv_empty = [&](int s) { return bar0 + 8u * (1 + kStages + s); };
-  auto s_full = [&](int b) { return bar0 + 8u * (1 + 2 * kStages + b); };
-  const uint32_t p_full = bar0 + 8u * (3 + 2 * kStages);
-  const uint32_t pv_done = bar0 + 8u * (4 + 2 * kStages);
-  const uint32_t drain = bar0 + 8u * (5 + 2 * kStages);
-  const uint32_t sQ = smem_u32(smem + kOffQ);
+  auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
+  auto sQ = [&](int x) { return smem_u32(smem + kOffQ + x * kQBytes); };
   auto sK = [&](int s) { return smem_u32(smem + kOffK + s * kKVBytes); };
   auto sV = [&](int s) { return smem_u32(smem + kOffV + s * kKVBytes); };
-  auto sP = [&](int b) { return smem_u32(smem + kOffP + b * kPBytes); };
+  auto sP = [&](int x) { return smem_u32(smem + kOffP + x * kPBytes); };
 
-  // Which image / query tile this CTA owns (launch order from the host).
+  // Which image / 256-row query block this CTA owns (launch order from the host).
   int slot = 0;
   while (slot + 1 < p.b.n_images && p.b.tile_start[slot + 1] <= static_cast<int>(blockIdx.x)) ++slot;
   const int img = p.b.order[slot];
   const int row0 = p.b.cu[img];
   const int len = p.b.cu[img + 1] - row0;
-  const int q0 = row0 + (static_cast<int>(blockIdx.x) - p.b.tile_start[slot]) * kTile;
-  const int q_valid = min(kTile, row0 + len - q0);
+  const int q0 = row0 + (static_cast<int>(blockIdx.x) - p.b.tile_start[slot]) * (2 * kTile);
   const int n_kv = (len + kTile - 1) / kTile;
   const int head = blockIdx.y;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(kv_full(s), 1);
-      mbar_init(kv_empty(s), 1);
+      mbar_init(bar(kBarKvFull + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 1);
     }
-    mbar_init(s_full(0), 1);
-    mbar_init(s_full(1), 1);
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
-    mbar_init(drain, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kBarSFull + x), 1);
+      mbar_init(bar(kBarSFree + x), 128);
+      mbar_init(bar(kBarPFull + x), 128);
+      mbar_init(bar(kBarPvDone + x), 1);
+    }
+    mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) prefetch_tensormap(&tm);
-  if (warp == 5) {
+  if (warp == 8 && lane == 0) prefetch_tensormap(&tm);
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -107,148 +144,188 @@ __global__ void __launch_bounds__(192, 1)
   int kv_issued = 0;
   bool q_issued = false;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(q_full, kQBytes);
-      tma_load_2d(sQ, &tm, q_full, head * kHd, q0);
+      mbar_expect_tx(bar(kBarQ), 2 * kQBytes);
+      tma_load_2d(sQ(0), &tm, bar(kBarQ), head * kHd, q0);
+      tma_load_2d(sQ(1), &tm, bar(kBarQ), head * kHd, q0 + kTile);
       q_issued = true;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % kStages;
-        if (!mbar_wait(kv_empty(s), ((j / kStages) & 1) ^ 1, p.status)) break;
-        mbar_expect_tx(kv_full(s), 2 * kKVBytes);
-        tma_load_2d(sK(s), &tm, kv_full(s), 1024 + head * kHd, row0 + j * kTile);
-        tma_load_2d(sV(s), &tm, kv_full(s), 2048 + head * kHd, row0 + j * kTile);
+        if (!mbar_wait(bar(kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, p.status)) break;
+        mbar_expect_tx(bar(kBarKvFull + s), 2 * kKVBytes);
+        tma_load_2d(sK(s), &tm, bar(kBarKvFull + s), 1024 + head * kHd, row0 + j * kTile);
+        tma_load_2d(sV(s), &tm, bar(kBarKvFull + s), 2048 + head * kHd, row0 + j * kTile);
         ++kv_issued;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
       int consumed = 0;
-      auto issue_s = [&](int j) {
+      auto issue_s = [&](int x, int j) {
         const int s = j % kStages;
-        const uint32_t d = tmem + (j & 1) * 128;
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
         for (int k = 0; k < kHd / 16; ++k)
-          umma_bf16(d, sdesc_sw128(sQ + k * 32, 16, 1024), sdesc_sw128(sK(s) + k * 32, 16, 1024),
+          umma_bf16(d, sdesc_sw128(sQ(x) + k * 32, 16, 1024), sdesc_sw128(sK(s) + k * 32, 16, 1024),
                     id_s, k != 0);
-        umma_commit(s_full(j & 1));
+        umma_commit(bar(kBarSFull + x));
       };
-      bool ok = mbar_wait(q_full, 0, p.status) && mbar_wait(kv_full(0), 0, p.status);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) {
-          const int s1 = (j + 1) % kStages;
-          if (!mbar_wait(kv_full(s1), ((j + 1) / kStages) & 1, p.status)) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
-        if (!mbar_wait(p_full, j & 1, p.status)) break;
-        tc_fence_after();
-        const int s = j % kStages;
-        const uint32_t pa = sP(j & 1), vb = sV(s);
+      auto issue_pv = [&](int x, int j) {
+        const uint32_t pa = sP(x), vb = sV(j % kStages);
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k) {
           const uint64_t a = sdesc_sw128(pa + (k >> 2) * (kPBytes / 2) + (k & 3) * 32, 16, 1024);
           const uint64_t b = sdesc_sw128(vb + k * 16 * 128, kKVBytes, 1024);
-          umma_bf16(tmem + kTmemO, a, b, id_o, (j | k) != 0);
+          umma_bf16(tmem + kTmemO + x * 64, a, b, id_o, (j | k) != 0);
         }
-        umma_commit(pv_done);
-        umma_commit(kv_empty(s));
+        umma_commit(bar(kBarPvDone + x));
+      };
+      bool ok = mbar_wait(bar(kBarQ), 0, p.status) && mbar_wait(bar(kBarKvFull), 0, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        issue_s(1, 0);
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const uint32_t par = j & 1;
+        if (j + 1 < n_kv) {
+          // The next scores of each tile as soon as its softmax has read the current ones.
+          if (!mbar_wait(bar(kBarKvFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, p.status)) break;
+          if (!mbar_wait(bar(kBarSFree + 0), par, p.status)) break;
+          tc_fence_after();
+          issue_s(0, j + 1);
+          if (!mbar_wait(bar(kBarSFree + 1), par, p.status)) break;
+          tc_fence_after();
+          issue_s(1, j + 1);
+        }
+        if (!mbar_wait(bar(kBarPFull + 0), par, p.status)) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (!mbar_wait(bar(kBarPFull + 1), par, p.status)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        umma_commit(bar(kBarKvEmpty + j % kStages));
         consumed = j + 1;
       }
       kv_consumed = consumed;
       // All MMAs of this CTA complete before TMEM is released.
-      umma_commit(drain);
-      mbar_wait(drain, 0, p.status);
+      umma_commit(bar(kBarDrain));
+      mbar_wait(bar(kBarDrain), 0, p.status);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int r = threadIdx.x;  // query row inside the tile == TMEM lane
-    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------------------------------------ softmax (warps 0-7)
+    const int x = warp >> 2;                 // query tile A (0) or B (1)
+    const int r = threadIdx.x & 127;         // row inside the tile == TMEM lane
+    const uint32_t lane_sel = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_sel;
+    const uint32_t tO = tmem + kTmemO + x * 64 + lane_sel;
+    const float c = p.scale_log2;
+    const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int b = j & 1;
-      if (!mbar_wait(s_full(b), (j >> 1) & 1, p.status)) {
+      const uint32_t par = j & 1;
+      if (!mbar_wait(bar(kBarSFull + x), par, p.status)) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t* dst = sr + 32 * c;
-        tmem_ld32(tmem + b * 128 + c * 32 + lane_sel, *reinterpret_cast<uint32_t(*)[32]>(dst));
-      }
+      for (int q = 0; q < 4; ++q)
+        tmem_ld32(tS + q * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * q));
       tmem_wait_ld();
-      const int kv_valid = min(kTile, len - j * kTile);
-      float mx = -INFINITY;
+      tc_fence_before();
+      mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
+      const int kv_valid = len - j * kTile;
+      if (kv_valid < kTile) {
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        const float x = (i < kv_valid) ? __uint_as_float(sr[i]) * p.scale_log2 : -INFINITY;
-        sr[i] = __float_as_uint(x);
-        mx = fmaxf(mx, x);
+        for (int i = 0; i < 128; ++i)
+          if (i >= kv_valid) sr[i] = __float_as_uint(-INFINITY);
       }
-      const float m_new = fmaxf(m, mx);
-      const float alpha = ex2_approx(m - m_new);
-      float sum = 0.f;
-      const uint32_t prow = sP(b) + r * 128;
+      float mx[8];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2_approx(__uint_as_float(sr[u * 8 + 2 * e]) - m_new);
-          const float p1 = ex2_approx(__uint_as_float(sr[u * 8 + 2 * e + 1]) - m_new);
-          sum += p0 + p1;
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        const uint32_t addr = prow + (u >> 3) * (kPBytes / 2) + (((u & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                     "r"(w[2]), "r"(w[3])
-                     : "memory");
+      for (int g = 0; g < 8; ++g) {
+        const uint32_t* v = sr + 16 * g;
+        float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+        a = max3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
+        a = max3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
+        a = max3(a, __uint_as_float(v[7]), __uint_as_float(v[8]));
+        a = max3(a, __uint_as_float(v[9]), __uint_as_float(v[10]));
+        a = max3(a, __uint_as_float(v[11]), __uint_as_float(v[12]));
+        a = max3(a, __uint_as_float(v[13]), __uint_as_float(v[14]));
+        mx[g] = fmaxf(a, __uint_as_float(v[15]));
       }
-      l = l * alpha + sum;
-      fence_proxy_async_smem();
+      const float m_tile =
+          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+      float m_new = m, alpha = 1.f;
+      if (m_tile > m + kRescaleThreshold) {   // always true on the first tile (m = -inf)
+        m_new = m_tile;
+        alpha = ex2_approx(m - m_new);
+      }
+      const uint64_t nm2 = f2(-m_new, -m_new);
+      uint64_t sum2 = f2(0.f, 0.f);
+      uint32_t pk[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const uint64_t t = f2_fma(f2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nm2);
+        float t0, t1;
+        f2_split(t, t0, t1);
+        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+        sum2 = f2_add(sum2, f2(p0, p1));
+        pk[i] = pack_bf16x2(p0, p1);
+      }
+      float s0, s1;
+      f2_split(sum2, s0, s1);
+      l = l * alpha + (s0 + s1);
       if (j > 0) {
-        if (!mbar_wait(pv_done, (j - 1) & 1, p.status)) {
+        // PV_X of the previous tile must be done: it read P_X, and O_X is rescaled below.
+        if (!mbar_wait(bar(kBarPvDone + x), par ^ 1, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xFFFFFFFFu, alpha < 1.f)) {
+      }
+      const uint32_t prow = sP(x) + r * 128;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + kTmemO + c * 32 + lane_sel, o);
-            tmem_wait_ld();
+      for (int u = 0; u < 16; ++u) {
+        const uint32_t addr = prow + (u >> 3) * (kPBytes / 2) + (((u & 7) ^ (r & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]),
+                     "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tmem + kTmemO + c * 32 + lane_sel, o);
-          }
-          tmem_wait_st();
+        for (int q = 0; q < 2; ++q) {
+          uint32_t o[32];
+          tmem_ld32(tO + q * 32, o);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + q * 32, o);
         }
+        tmem_wait_st();
       }
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(bar(kBarPFull + x));
       m = m_new;
     }
-    if (ok && n_kv > 0 && mbar_wait(pv_done, (n_kv - 1) & 1, p.status)) {
+    if (ok && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
       const float inv_l = 1.f / l;
       uint32_t o[64];
-      tmem_ld32(tmem + kTmemO + lane_sel, *reinterpret_cast<uint32_t(*)[32]>(o));
-      tmem_ld32(tmem + kTmemO + 32 + lane_sel, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+      tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
+      tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
       tmem_wait_ld();
-      if (r < q_valid) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(q0 + r) * 1024 + head * kHd);
+      const int qrow = q0 + x * kTile + r;
+      if (qrow < row0 + len) {
+        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * 1024 + head * kHd);
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           dst[q] = make_uint4(
@@ -263,13 +340,15 @@ __global__ void __launch_bounds__(192, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0 && status_failed(p.status)) {
-    if (q_issued) mbar_wait(q_full, 0, nullptr);
+  if (warp == 8 && lane == 0 && status_failed(p.status)) {
+    // After a timeout: wait (bounded) for the loads still in flight, so no TMA
+    // write lands in shared memory after the CTA has exited.
+    if (q_issued) mbar_wait(bar(kBarQ), 0, nullptr);
     for (int j = kv_consumed; j < kv_issued; ++j)
-      if (!mbar_wait(kv_full(j % kStages), (j / kStages) & 1, nullptr)) break;
+      if (!mbar_wait(bar(kBarKvFull + j % kStages), (j / kStages) & 1, nullptr)) break;
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -291,9 +370,9 @@ int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* ou
   p.out = out;
   p.status = status;
   p.scale_log2 = 1.4426950408889634f * 0.125f;
-  const int tiles = batch.tile_start[batch.n_images];
-  if (tiles <= 0) return DS_VIT_OK;
-  attn_kernel<<<dim3(tiles, 16), 192, kSmemBytes, stream>>>(tm_qkv, p);
+  const int ctas = batch.tile_start[batch.n_images];
+  if (ctas <= 0) return DS_VIT_OK;
+  attn_kernel<<<dim3(ctas, 16), kThreads, kSmemBytes, stream>>>(tm_qkv, p);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 

@@ -32,10 +32,13 @@ int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, in
 // The BN that launch_gemm uses for an N-wide output (the B tensor map's box rows).
 int gemm_bn(int M, int N);
 
+// Query rows per attention CTA (two 128-row tiles).
+constexpr int kAttnRowsPerCta = 256;
+
 struct AttnBatch {
   int n_images;
   int cu[DS_VIT_MAX_IMAGES + 1];          // packed row offsets of the images
-  int tile_start[DS_VIT_MAX_IMAGES + 1];  // q-tile prefix sums in launch order
+  int tile_start[DS_VIT_MAX_IMAGES + 1];  // CTA prefix sums (kAttnRowsPerCta rows each), launch order
   int order[DS_VIT_MAX_IMAGES];           // launch slot -> image index
 };
 

@@ -179,6 +179,11 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
       !make_tmap_bf16(&tA_m, h, T, 9216, 128) || !make_tmap_bf16(&tA_u, qkv, T, 5120, 128) ||
       !make_tmap_bf16(&t_qkv, qkv, N, 3072, 128))
     return DS_VIT_ECUDA;
+  CUtensorMap tC_x, tC_qkv, tC_h, tC_u, tC_out;
+  if (!make_tmap_store_bf16(&tC_x, x, N, 1024) || !make_tmap_store_bf16(&tC_qkv, qkv, N, 3072) ||
+      !make_tmap_store_bf16(&tC_h, h, N, 4096) || !make_tmap_store_bf16(&tC_u, qkv, T, 5120) ||
+      !make_tmap_store_bf16(&tC_out, out, T, 5120))
+    return DS_VIT_ECUDA;
   for (int i = 0; i <= n; ++i) tok_offsets[i] = ib.tok_off[i];
 
   PixelNorm norm;
@@ -208,7 +213,7 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
   } while (0)
   DSV_LAUNCH(DS_VIT_KERNEL_IM2COL, launch_im2col(ib, norm, h, rowpos, st));
   DSV_LAUNCH(DS_VIT_KERNEL_PATCH_GEMM,
-             launch_gemm(tA_pe, p->tm_patch, N, 1024, 640, static_cast<const bf16*>(w.patch_b), x,
+             launch_gemm(tA_pe, p->tm_patch, tC_x, N, 1024, 640, static_cast<const bf16*>(w.patch_b), x,
                          kEpiBias, nullptr, nullptr, p->status, st));
   if (dump_blocks) DSV_CUDA(cudaMemcpyAsync(dump_blocks, x, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
   for (int l = 0; l < cfg.n_layers; ++l) {
@@ -217,20 +222,20 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
                launch_layernorm(x, static_cast<const bf16*>(L.ln1_g),
                                 static_cast<const bf16*>(L.ln1_b), y, N, cfg.ln_eps, st));
     DSV_LAUNCH(DS_VIT_KERNEL_QKV_GEMM,
-               launch_gemm(tA_y, p->tm_qkv[l], N, 3072, 1024, static_cast<const bf16*>(L.qkv_b),
+               launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, 3072, 1024, static_cast<const bf16*>(L.qkv_b),
                            qkv, kEpiQkvRope, rowpos, p->rope_cs, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_ATTENTION, launch_attention(t_qkv, ab, o, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_PROJ_GEMM,
-               launch_gemm(tA_o, p->tm_proj[l], N, 1024, 1024, static_cast<const bf16*>(L.proj_b),
+               launch_gemm(tA_o, p->tm_proj[l], tC_x, N, 1024, 1024, static_cast<const bf16*>(L.proj_b),
                            x, kEpiBiasResid, nullptr, nullptr, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_LAYERNORM,
                launch_layernorm(x, static_cast<const bf16*>(L.ln2_g),
                                 static_cast<const bf16*>(L.ln2_b), y, N, cfg.ln_eps, st));
     DSV_LAUNCH(DS_VIT_KERNEL_FC1_GEMM,
-               launch_gemm(tA_y, p->tm_fc1[l], N, 4096, 1024, static_cast<const bf16*>(L.fc1_b), h,
+               launch_gemm(tA_y, p->tm_fc1[l], tC_h, N, 4096, 1024, static_cast<const bf16*>(L.fc1_b), h,
                            kEpiBiasGelu, nullptr, nullptr, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_FC2_GEMM,
-               launch_gemm(tA_h, p->tm_fc2[l], N, 1024, 4096, static_cast<const bf16*>(L.fc2_b), x,
+               launch_gemm(tA_h, p->tm_fc2[l], tC_x, N, 1024, 4096, static_cast<const bf16*>(L.fc2_b), x,
                            kEpiBiasResid, nullptr, nullptr, p->status, st));
     if (dump_blocks)
       DSV_CUDA(cudaMemcpyAsync(dump_blocks + (l + 1) * N * 1024, x, N * 1024 * 2,
@@ -242,10 +247,10 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
   if (dump_final) DSV_CUDA(cudaMemcpyAsync(dump_final, y, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGE_GATHER, launch_merge_gather(ib, y, h, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGER_GEMM1,
-             launch_gemm(tA_m, p->tm_m1, T, 5120, 9216, static_cast<const bf16*>(w.m1_b), qkv,
+             launch_gemm(tA_m, p->tm_m1, tC_u, T, 5120, 9216, static_cast<const bf16*>(w.m1_b), qkv,
                          kEpiBiasGelu, nullptr, nullptr, p->status, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGER_GEMM2,
-             launch_gemm(tA_u, p->tm_m2, T, 5120, 5120, static_cast<const bf16*>(w.m2_b), out,
+             launch_gemm(tA_u, p->tm_m2, tC_out, T, 5120, 5120, static_cast<const bf16*>(w.m2_b), out,
                          kEpiBias, nullptr, nullptr, p->status, st));
 #undef DSV_LAUNCH
   if (p->t_count) *p->t_count = n_timed < p->t_slots ? n_timed : p->t_slots;
@@ -515,10 +520,11 @@ int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t
     return DS_VIT_EINVAL;
   if (epilogue == kEpiQkvRope && (N != 3072 || !rowpos || !rope_cs)) return DS_VIT_EINVAL;
   if (!aligned16(a) || !aligned16(w) || !aligned16(bias) || !aligned16(out)) return DS_VIT_EINVAL;
-  CUtensorMap tA, tB;
-  if (!make_tmap_bf16(&tA, a, M, K, 128) || !make_tmap_bf16(&tB, w, N, K, gemm_bn(M, N)))
+  CUtensorMap tA, tB, tC;
+  if (!make_tmap_bf16(&tA, a, M, K, 128) || !make_tmap_bf16(&tB, w, N, K, gemm_bn(M, N)) ||
+      !make_tmap_store_bf16(&tC, out, M, N))
     return DS_VIT_ECUDA;
-  return launch_gemm(tA, tB, static_cast<int>(M), N, K, static_cast<const bf16*>(bias),
+  return launch_gemm(tA, tB, tC, static_cast<int>(M), N, K, static_cast<const bf16*>(bias),
                      static_cast<bf16*>(out), epilogue, rowpos, rope_cs, status,
                      static_cast<cudaStream_t>(stream));
 }

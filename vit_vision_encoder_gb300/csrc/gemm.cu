@@ -3,7 +3,7 @@
 // A [M, K] (activations) and B [N, K] (nn.Linear weights) are both K-major
 // bf16, staged by TMA into 128-byte-swizzled shared-memory tiles; one thread
 // issues tcgen05.mma (M = 128, N = BN, K = 16 per instruction) into a TMEM
-// accumulator; four epilogue warps read it back with tcgen05.ld and apply the
+// accumulator; eight epilogue warps read it back with tcgen05.ld and apply the
 // fused epilogue:
 //   bias                 — patch projection ("Multimodal basics": a patch
 //                          projection maps pixel rows into the vision hidden
@@ -18,11 +18,14 @@
 //                          width occupy blocks in 2D RoPE").
 // All from "DeepSeek V4.1 Flash Engineering, Part 3: Integrating Vision".
 //
-// Structure: persistent CTAs (one per SM), 6 warps: warps 0-3 epilogue (TMEM
-// lane quadrant = warp index), warp 4 TMA producer, warp 5 MMA issuer.  A ring
-// of STAGES shared-memory stages (full/empty mbarriers) feeds the MMA; two TMEM
+// Structure: persistent CTAs (one per SM), 10 warps: warps 0-7 epilogue (TMEM
+// lane quadrant = warp % 4; warps 0-3 take the even 32-column chunks of a tile,
+// warps 4-7 the odd ones), warp 8 TMA producer, warp 9 MMA issuer.  A ring of
+// STAGES shared-memory stages (full/empty mbarriers) feeds the MMA; two TMEM
 // accumulators (tfull/tempty mbarriers) let the epilogue of one tile overlap
-// the main loop of the next.
+// the main loop of the next.  The tile's bias is staged once in shared memory;
+// each 32x32 output chunk goes through a 64-byte-swizzled shared staging tile
+// (two per warp) and leaves by TMA store, which also clips rows past M.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -36,7 +39,7 @@ namespace {
 
 struct GemmParams {
   int M, N, K;
-  bf16* out;
+  bf16* out;          // read by the residual epilogue; written through tmC
   const bf16* bias;
   const int* rowpos;
   const float* rope_cs;
@@ -50,26 +53,32 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  static constexpr int STAGES = 4;
+  static constexpr int EPI_WARPS = 8;
+  static constexpr int STG_BYTES = 32 * 32 * 2;                // one 32x32 bf16 chunk
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;         // 2 staging chunks per warp
+  static constexpr int OFF_BIAS = OFF_STG + EPI_WARPS * 2 * STG_BYTES;
+  static constexpr int OFF_BAR = OFF_BIAS + 2 * BN * 2;        // bias, double-buffered by tile
+  static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;      // + barriers + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int SMEM_BYTES = BAR_OFF + 256 + 1024;  // + barriers + alignment slack
+  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
 };
+static_assert(GemmCfg<256>::SMEM_BYTES <= 232448, "shared memory");
 
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
 template <int BN, int EPI>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 31);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
@@ -92,16 +101,17 @@ __global__ void __launch_bounds__(192, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 4);
+      mbar_init(tempty_bar(a), C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     fence_barrier_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmC);
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -113,7 +123,7 @@ __global__ void __launch_bounds__(192, 1)
   __shared__ int consumed_fills;
   int issued_fills = 0;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       int stage = 0;
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(192, 1)
         if (!ok) break;
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false, false);
@@ -179,97 +189,138 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(drain_bar, 0, p.status);
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-3)
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    const int grp = warp >> 2;                   // chunk parity this warp handles
+    const int quad = warp & 3;                   // TMEM lane quadrant = 32-row slice
+    const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
+    const uint32_t stg0 = smem_u32(smem + C::OFF_STG + warp * 2 * C::STG_BYTES);
+    const uint32_t bias_s = smem_u32(smem + C::OFF_BIAS);
     uint32_t acc = 0, acc_phase = 0;
-    const uint32_t lane_sel = static_cast<uint32_t>(warp * 32) << 16;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+    int stg = 0, it = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
       const int mb = tile % num_m, nb = tile / num_m;
-      if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
-      tc_fence_after();
-      const int row = mb * C::BM + warp * 32 + lane;
-      const bool valid = row < p.M;
-      int gy = 0, gx = 0;
-      if constexpr (EPI == kEpiQkvRope) {
-        if (valid) {
-          const int rp = __ldg(p.rowpos + row);
-          gy = rp >> 16;
-          gx = rp & 0xFFFF;
+      // The tile's bias -> shared memory (buffer it & 1), by warp 0.
+      const uint32_t bias_buf = bias_s + (it & 1) * (BN * 2);
+      if (warp == 0) {
+#pragma unroll
+        for (int q = lane; q < BN / 8; q += 32) {
+          const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + nb * BN) + q);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bias_buf + q * 16), "r"(b.x),
+                       "r"(b.y), "r"(b.z), "r"(b.w)
+                       : "memory");
         }
       }
+      named_barrier(1, C::EPI_WARPS * 32);
+      const int row0 = mb * C::BM + quad * 32;
+      const int row = row0 + lane;
+      const bool valid = row < p.M;
+      // RoPE: warps of group 0 hold head dims 0..31 (patch row), group 1 dims
+      // 32..63 (patch column); all columns of a tile below 2048 are q or k.
+      float rc[16], rs[16];
+      bool rotate = false;
+      if constexpr (EPI == kEpiQkvRope) {
+        rotate = nb * BN < 2048;
+        if (rotate) {
+          int pos = 0;
+          if (valid) {
+            const int rp = __ldg(p.rowpos + row);
+            pos = grp == 0 ? (rp >> 16) : (rp & 0xFFFF);
+          }
+          const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + pos * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float4 a = __ldg(cs + q), b = __ldg(cs + 4 + q);
+            rc[4 * q] = a.x; rc[4 * q + 1] = a.y; rc[4 * q + 2] = a.z; rc[4 * q + 3] = a.w;
+            rs[4 * q] = b.x; rs[4 * q + 1] = b.y; rs[4 * q + 2] = b.z; rs[4 * q + 3] = b.w;
+          }
+        }
+      }
+      if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
+      tc_fence_after();
 #pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
+      for (int cc = 0; cc < BN / 64; ++cc) {
+        const int c = 2 * cc + grp;
+        const int n0 = nb * BN + c * 32;
+        uint4 rx[4];
+        if constexpr (EPI == kEpiBiasResid) {
+          const uint4* src = reinterpret_cast<const uint4*>(p.out + static_cast<size_t>(row) * p.N + n0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rx[q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
+        }
         uint32_t r[32];
         tmem_ld32(tmem_base + acc * BN + c * 32 + lane_sel, r);
         tmem_wait_ld();
-        if (c == BN / 32 - 1) {
+        if (cc == BN / 64 - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
         }
-        const int n0 = nb * BN + c * 32;
         float v[32];
-        const uint4* bias4 = reinterpret_cast<const uint4*>(p.bias + n0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint4 b = __ldg(bias4 + q);
-          const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+          uint32_t bw[4];
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
+                       : "r"(bias_buf + c * 64 + q * 16));
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             v[q * 8 + 2 * e] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e]), bf16lo(bw[e]));
             v[q * 8 + 2 * e + 1] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e + 1]), bf16hi(bw[e]));
           }
         }
-        bf16* dst = p.out + static_cast<size_t>(row) * p.N + n0;
         if constexpr (EPI == kEpiBiasGelu) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
         } else if constexpr (EPI == kEpiBiasResid) {
-          if (valid) {
-            const uint4* src = reinterpret_cast<const uint4*>(dst);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const uint4 x = src[q];
-              const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t xw[4] = {rx[q].x, rx[q].y, rx[q].z, rx[q].w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                v[q * 8 + 2 * e] = __fadd_rn(bf16lo(xw[e]), v[q * 8 + 2 * e]);
-                v[q * 8 + 2 * e + 1] = __fadd_rn(bf16hi(xw[e]), v[q * 8 + 2 * e + 1]);
-              }
+            for (int e = 0; e < 4; ++e) {
+              v[q * 8 + 2 * e] = __fadd_rn(bf16lo(xw[e]), v[q * 8 + 2 * e]);
+              v[q * 8 + 2 * e + 1] = __fadd_rn(bf16hi(xw[e]), v[q * 8 + 2 * e + 1]);
             }
           }
         } else if constexpr (EPI == kEpiQkvRope) {
-          if (n0 < 2048) {
-            // 32 columns = one rotary half of one head: dims 0..31 -> row, 32..63 -> column.
-            const int pos = ((n0 >> 5) & 1) ? gx : gy;
-            const float* cs = p.rope_cs + pos * 32;
+          if (rotate) {
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-              const float cj = __ldg(cs + j), sj = __ldg(cs + 16 + j);
               const float a = v[j], b = v[j + 16];
-              v[j] = __fsub_rn(__fmul_rn(a, cj), __fmul_rn(b, sj));
-              v[j + 16] = __fadd_rn(__fmul_rn(b, cj), __fmul_rn(a, sj));
+              v[j] = __fsub_rn(__fmul_rn(a, rc[j]), __fmul_rn(b, rs[j]));
+              v[j + 16] = __fadd_rn(__fmul_rn(b, rc[j]), __fmul_rn(a, rs[j]));
             }
           }
         }
-        if (valid) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst);
+        // Stage the 32x32 chunk (64-byte swizzle: 16-byte unit q of row r at
+        // unit q ^ ((r >> 1) & 3)) and store it with TMA.
+        const uint32_t buf = stg0 + stg * C::STG_BYTES;
+        if (lane == 0) bulk_wait_read<1>();        // this buffer's previous store has read it
+        __syncwarp();
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            d4[q] = make_uint4(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1]),
-                               pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3]),
-                               pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5]),
-                               pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]));
-          }
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t addr = buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                       "r"(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1])), "r"(pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3])),
+                       "r"(pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5])), "r"(pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]))
+                       : "memory");
         }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && row0 < p.M) {
+          tma_store_2d(&tmC, buf, n0, row0);
+          bulk_commit();
+        }
+        stg ^= 1;
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 4 && lane == 0 && status_failed(p.status)) {
+  if (warp == 8 && lane == 0 && status_failed(p.status)) {
     // After a timeout: wait (bounded) for the tile loads still in flight, so no
     // TMA write lands in shared memory after the CTA has exited.
     for (int f = consumed_fills; f < issued_fills; ++f) {
@@ -278,15 +329,15 @@ __global__ void __launch_bounds__(192, 1)
     }
   }
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
 }
 
 template <int BN, int EPI>
-int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                  cudaStream_t stream) {
+int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
+                  const GemmParams& p, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -297,8 +348,36 @@ int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmPara
   if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
   const int tiles = ((p.M + 127) / 128) * (p.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<BN, EPI><<<grid, 192, C::SMEM_BYTES, stream>>>(tmA, tmB, p);
+  gemm_kernel<BN, EPI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return encode;
+}
+
+bool encode_tmap(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                 uint32_t box_cols, uint32_t box_rows, CUtensorMapSwizzle swz) {
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+  if (!encode || !base || rows == 0 || cols == 0) return false;
+  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -316,40 +395,25 @@ int num_sms() {
 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  if (!encode || !base || rows == 0 || cols == 0) return false;
-  if ((reinterpret_cast<uintptr_t>(base) & 15) != 0 || (cols * 2) % 16 != 0) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return encode_tmap(map, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+  return encode_tmap(map, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 int gemm_bn(int /*M*/, int /*N*/) { return 256; }
 
-int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                const bf16* bias, bf16* out, int epi, const int* rowpos, const float* rope_cs,
-                int* status, cudaStream_t stream) {
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M,
+                int N, int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
+                const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
   GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status};
   switch (epi) {
-    case kEpiBias: return launch_gemm_t<256, kEpiBias>(tmA, tmB, p, stream);
-    case kEpiBiasGelu: return launch_gemm_t<256, kEpiBiasGelu>(tmA, tmB, p, stream);
-    case kEpiBiasResid: return launch_gemm_t<256, kEpiBiasResid>(tmA, tmB, p, stream);
-    case kEpiQkvRope: return launch_gemm_t<256, kEpiQkvRope>(tmA, tmB, p, stream);
+    case kEpiBias: return launch_gemm_t<256, kEpiBias>(tmA, tmB, tmC, p, stream);
+    case kEpiBiasGelu: return launch_gemm_t<256, kEpiBiasGelu>(tmA, tmB, tmC, p, stream);
+    case kEpiBiasResid: return launch_gemm_t<256, kEpiBiasResid>(tmA, tmB, tmC, p, stream);
+    case kEpiQkvRope: return launch_gemm_t<256, kEpiQkvRope>(tmA, tmB, tmC, p, stream);
     default: return DS_VIT_EINVAL;
   }
 }

@@ -21,13 +21,17 @@ enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkv
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
+// Store map of a row-major bf16 output [rows, cols]: 32x32 boxes, 64-byte swizzle.
+bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
+
 int num_sms();
 
-// out[M, N] = epi(A[M, K] B[N, K]^T + bias); tmB describes B with box rows == BN.
-// Returns DS_VIT_OK or DS_VIT_ECUDA.
-int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, int M, int N, int K,
-                const bf16* bias, bf16* out, int epi, const int* rowpos, const float* rope_cs,
-                int* status, cudaStream_t stream);
+// out[M, N] = epi(A[M, K] B[N, K]^T + bias); tmB describes B with box rows == BN,
+// tmC is the store map of `out` (make_tmap_store_bf16).  Returns DS_VIT_OK or
+// DS_VIT_ECUDA.
+int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M,
+                int N, int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
+                const float* rope_cs, int* status, cudaStream_t stream);
 
 // The BN that launch_gemm uses for an N-wide output (the B tensor map's box rows).
 int gemm_bn(int M, int N);

@@ -10,17 +10,18 @@
 // One CTA = one (image, 256 query rows, head), as two 128-row query tiles A
 // and B that share every K/V tile.  Warps 0-3 run the softmax of tile A and
 // warps 4-7 that of tile B (one query row per thread, TMEM lane = row); warp 8
-// loads Q once and streams K/V tiles of 128 rows through a 3-stage TMA ring;
-// warp 9 issues the MMAs:
-//   S_X = Q_X K_j^T     (M 128, N 128, K 64)  -> TMEM, one buffer per tile X
-//   O_X += P_X V_j      (M 128, N 64,  K 128) -> TMEM
+// loads Q once and streams K/V tiles of 128 rows through a 4-stage TMA ring;
+// warp 9 issues the MMAs of tile A and warp 10 those of tile B, so the two
+// tiles proceed independently on the tensor core:
+//   S_X = Q_X K_j^T     (M 128, N 128, K 64)  smem x smem -> TMEM
+//   O_X += P_X V_j      (M 128, N 64,  K 128) TMEM x smem -> TMEM
 // A softmax warpgroup reads S_X from TMEM and hands the buffer back at once,
-// so the next S_X is computed while it works; the two warpgroups alternate
-// on the tensor core.  The running row maximum m (exp2 domain) is raised only
-// when a tile's maximum exceeds it by more than 8, so P = exp2(s - m) stays
-// below 2^8 and O is rescaled (in TMEM, by exp2(m_old - m_new)) rarely; the
-// final O / l uses the same m, so the result is the exact softmax.  P is
-// written as bf16 into a 128-byte-swizzled shared tile, the PV MMA's A operand.
+// so the next S_X is computed while it works.  The running row maximum m
+// (exp2 domain) is raised only when a tile's maximum exceeds it by more than
+// 8, so P = exp2(s - m) stays below 2^8 and O is rescaled (in TMEM, by
+// exp2(m_old - m_new)) rarely; the final O / l uses the same m, so the result
+// is the exact softmax.  P is written as bf16 pairs into TMEM, where the PV
+// MMA reads its A operand.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -32,19 +33,20 @@ namespace {
 
 constexpr int kTile = 128;     // rows of a query tile and of a K/V tile
 constexpr int kHd = 64;        // head dim
-constexpr int kStages = 3;     // K/V ring depth
+constexpr int kStages = 4;     // K/V ring depth
 constexpr int kQBytes = kTile * kHd * 2;              // 16 KB per query tile
 constexpr int kKVBytes = kTile * kHd * 2;             // 16 KB each for K and V
-constexpr int kPBytes = kTile * kTile * 2;            // 32 KB (two 64-column chunks)
 constexpr int kOffQ = 0;                              // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kQBytes;
 constexpr int kOffV = kOffK + kStages * kKVBytes;
-constexpr int kOffP = kOffV + kStages * kKVBytes;     // P_A, P_B
-constexpr int kOffBar = kOffP + 2 * kPBytes;
+constexpr int kOffBar = kOffV + kStages * kKVBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
-constexpr uint32_t kTmemCols = 512;   // S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384)
+// TMEM columns: S_A [0,128), S_B [128,256), O_A [256,320), O_B [320,384),
+// P_A [384,448), P_B [448,512) (P as packed bf16 pairs).
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
-constexpr int kThreads = 320;         // 8 softmax warps, TMA warp, MMA warp
+constexpr uint32_t kTmemP = 384;
+constexpr int kThreads = 352;         // 8 softmax warps, TMA warp, 2 MMA warps
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays below 2^8
 
 // Barrier slots (8 bytes each).
@@ -54,8 +56,8 @@ enum : int {
   kBarSFree = kBarSFull + 2,           // [2]
   kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
-  kBarDrain = kBarPvDone + 2,
-  kBarCount = kBarDrain + 1
+  kBarDrain = kBarPvDone + 2,          // [2]
+  kBarCount = kBarDrain + 2
 };
 static_assert(kBarCount <= 30, "barrier area");
 
@@ -90,6 +92,8 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
+// Registers are split per SM sub-partition: with 11 warps three of them share
+// one sub-partition's 16K registers, which caps a thread at 168.
 __global__ void __launch_bounds__(kThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -102,7 +106,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto sQ = [&](int x) { return smem_u32(smem + kOffQ + x * kQBytes); };
   auto sK = [&](int s) { return smem_u32(smem + kOffK + s * kKVBytes); };
   auto sV = [&](int s) { return smem_u32(smem + kOffV + s * kKVBytes); };
-  auto sP = [&](int x) { return smem_u32(smem + kOffP + x * kPBytes); };
 
   // Which image / 256-row query block this CTA owns (launch order from the host).
   int slot = 0;
@@ -119,15 +122,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
-      mbar_init(bar(kBarKvEmpty + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 2);      // released by both MMA warps
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(kBarSFull + x), 1);
       mbar_init(bar(kBarSFree + x), 128);
       mbar_init(bar(kBarPFull + x), 128);
       mbar_init(bar(kBarPvDone + x), 1);
+      mbar_init(bar(kBarDrain + x), 1);
     }
-    mbar_init(bar(kBarDrain), 1);
     fence_barrier_init();
   }
   if (warp == 8 && lane == 0) prefetch_tensormap(&tm);
@@ -140,7 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  __shared__ int kv_consumed;
+  __shared__ int kv_consumed[2];
   int kv_issued = 0;
   bool q_issued = false;
 
@@ -160,62 +163,51 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kv_issued;
       }
     }
-  } else if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp >= 9) {
+    // ------------------------------------------------------------ MMA issuer of tile X
+    const int x = warp - 9;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
+      const uint32_t tS = tmem + x * 128, tO = tmem + kTmemO + x * 64, tP = tmem + kTmemP + x * 64;
       int consumed = 0;
-      auto issue_s = [&](int x, int j) {
-        const int s = j % kStages;
-        const uint32_t d = tmem + x * 128;
+      auto issue_s = [&](int j) {
+        const uint32_t k0 = sK(j % kStages);
 #pragma unroll
         for (int k = 0; k < kHd / 16; ++k)
-          umma_bf16(d, sdesc_sw128(sQ(x) + k * 32, 16, 1024), sdesc_sw128(sK(s) + k * 32, 16, 1024),
+          umma_bf16(tS, sdesc_sw128(sQ(x) + k * 32, 16, 1024), sdesc_sw128(k0 + k * 32, 16, 1024),
                     id_s, k != 0);
         umma_commit(bar(kBarSFull + x));
-      };
-      auto issue_pv = [&](int x, int j) {
-        const uint32_t pa = sP(x), vb = sV(j % kStages);
-#pragma unroll
-        for (int k = 0; k < kTile / 16; ++k) {
-          const uint64_t a = sdesc_sw128(pa + (k >> 2) * (kPBytes / 2) + (k & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(vb + k * 16 * 128, kKVBytes, 1024);
-          umma_bf16(tmem + kTmemO + x * 64, a, b, id_o, (j | k) != 0);
-        }
-        umma_commit(bar(kBarPvDone + x));
       };
       bool ok = mbar_wait(bar(kBarQ), 0, p.status) && mbar_wait(bar(kBarKvFull), 0, p.status);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        issue_s(1, 0);
+        issue_s(0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
         const uint32_t par = j & 1;
         if (j + 1 < n_kv) {
-          // The next scores of each tile as soon as its softmax has read the current ones.
+          // The next scores as soon as the softmax has read the current ones.
           if (!mbar_wait(bar(kBarKvFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, p.status)) break;
-          if (!mbar_wait(bar(kBarSFree + 0), par, p.status)) break;
+          if (!mbar_wait(bar(kBarSFree + x), par, p.status)) break;
           tc_fence_after();
-          issue_s(0, j + 1);
-          if (!mbar_wait(bar(kBarSFree + 1), par, p.status)) break;
-          tc_fence_after();
-          issue_s(1, j + 1);
+          issue_s(j + 1);
         }
-        if (!mbar_wait(bar(kBarPFull + 0), par, p.status)) break;
+        if (!mbar_wait(bar(kBarPFull + x), par, p.status)) break;
         tc_fence_after();
-        issue_pv(0, j);
-        if (!mbar_wait(bar(kBarPFull + 1), par, p.status)) break;
-        tc_fence_after();
-        issue_pv(1, j);
+        const uint32_t vb = sV(j % kStages);
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k)
+          umma_bf16_ts(tO, tP + k * 8, sdesc_sw128(vb + k * 16 * 128, kKVBytes, 1024), id_o,
+                       (j | k) != 0);
+        umma_commit(bar(kBarPvDone + x));
         umma_commit(bar(kBarKvEmpty + j % kStages));
         consumed = j + 1;
       }
-      kv_consumed = consumed;
-      // All MMAs of this CTA complete before TMEM is released.
-      umma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, p.status);
+      kv_consumed[x] = consumed;
+      // All MMAs of this warp complete before TMEM is released.
+      umma_commit(bar(kBarDrain + x));
+      mbar_wait(bar(kBarDrain + x), 0, p.status);
     }
   } else {
     // ------------------------------------------------------------ softmax (warps 0-7)
@@ -224,6 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_sel = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tmem + x * 128 + lane_sel;
     const uint32_t tO = tmem + kTmemO + x * 64 + lane_sel;
+    const uint32_t tP = tmem + kTmemP + x * 64 + lane_sel;
     const float c = p.scale_log2;
     const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
@@ -269,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2_approx(m - m_new);
       }
       const uint64_t nm2 = f2(-m_new, -m_new);
-      uint64_t sum2 = f2(0.f, 0.f);
+      uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
@@ -277,11 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         float t0, t1;
         f2_split(t, t0, t1);
         const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
-        sum2 = f2_add(sum2, f2(p0, p1));
+        acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
+      const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float s0, s1;
-      f2_split(sum2, s0, s1);
+      f2_split(s2, s0, s1);
       l = l * alpha + (s0 + s1);
       if (j > 0) {
         // PV_X of the previous tile must be done: it read P_X, and O_X is rescaled below.
@@ -291,15 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
       }
-      const uint32_t prow = sP(x) + r * 128;
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const uint32_t addr = prow + (u >> 3) * (kPBytes / 2) + (((u & 7) ^ (r & 7)) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(pk[4 * u]),
-                     "r"(pk[4 * u + 1]), "r"(pk[4 * u + 2]), "r"(pk[4 * u + 3])
-                     : "memory");
-      }
-      fence_proxy_async_smem();
+      tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
@@ -310,8 +297,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tO + q * 32, o);
         }
-        tmem_wait_st();
       }
+      tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + x));
       m = m_new;
@@ -344,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // After a timeout: wait (bounded) for the loads still in flight, so no TMA
     // write lands in shared memory after the CTA has exited.
     if (q_issued) mbar_wait(bar(kBarQ), 0, nullptr);
-    for (int j = kv_consumed; j < kv_issued; ++j)
+    const int done = kv_consumed[0] < kv_consumed[1] ? kv_consumed[0] : kv_consumed[1];
+    for (int j = done; j < kv_issued; ++j)
       if (!mbar_wait(bar(kBarKvFull + j % kStages), (j / kStages) & 1, nullptr)) break;
   }
   __syncthreads();

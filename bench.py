@@ -240,7 +240,8 @@ def run_profile_case(case: str):
         run = lambda: dv.op_attention(qkv, [N_PATCH], out=o)
     elif case.startswith("gemm-"):
         K, N, epi = {"gemm-qkv": (1024, 3072, dv.EPI_BIAS), "gemm-fc1": (1024, 4096, dv.EPI_BIAS_GELU),
-                     "gemm-fc2": (4096, 1024, dv.EPI_BIAS_RESID)}[case]
+                     "gemm-fc2": (4096, 1024, dv.EPI_BIAS_RESID),
+                     "gemm-proj": (1024, 1024, dv.EPI_BIAS_RESID)}[case]
         a = torch.randn((N_PATCH, K), device="cuda").to(torch.bfloat16)
         w = (torch.randn((N, K), device="cuda") * 0.02).to(torch.bfloat16)
         b = torch.zeros(N, device="cuda").to(torch.bfloat16)

@@ -14,48 +14,63 @@ namespace {
 // coalesced across the warp).  fp32 statistics: mean, then the biased variance
 // of the centred values; y = (x - mu) * (1/sqrt(var + eps)) * g + b rounded to
 // bf16 ("Step 2": the final-norm boundary; block pre-norms).
-__global__ void __launch_bounds__(256) layernorm_kernel(const bf16* __restrict__ x,
+__global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ x,
                                                         const bf16* __restrict__ g,
                                                         const bf16* __restrict__ b,
                                                         bf16* __restrict__ y, int64_t M,
                                                         float eps) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   if (row >= M) return;
+  // Every load of the row (x, gamma, beta) is issued before any arithmetic.
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * 1024);
+  const uint4* g4 = reinterpret_cast<const uint4*>(g);
+  const uint4* b4 = reinterpret_cast<const uint4*>(b);
+  uint4 xu[4], gu[4], bu[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) xu[q] = __ldg(xr + q * 32 + lane);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    gu[q] = __ldg(g4 + q * 32 + lane);
+    bu[q] = __ldg(b4 + q * 32 + lane);
+  }
   float v[32];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 u = xr[q * 32 + lane];
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t w[4] = {xu[q].x, xu[q].y, xu[q].z, xu[q].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       v[q * 8 + 2 * e] = bf16lo(w[e]);
       v[q * 8 + 2 * e + 1] = bf16hi(w[e]);
     }
   }
-  float s = 0.f;
+  float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) s += v[i];
+  for (int i = 0; i < 32; i += 2) {
+    s0 += v[i];
+    s1 += v[i + 1];
+  }
+  float s = s0 + s1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
   const float mu = __fdiv_rn(s, 1024.f);
-  float ss = 0.f;
+  float q0 = 0.f, q1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < 32; i += 2) {
     v[i] = __fsub_rn(v[i], mu);
-    ss = __fmaf_rn(v[i], v[i], ss);
+    v[i + 1] = __fsub_rn(v[i + 1], mu);
+    q0 = __fmaf_rn(v[i], v[i], q0);
+    q1 = __fmaf_rn(v[i + 1], v[i + 1], q1);
   }
+  float ss = q0 + q1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
   const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1024.f), eps)));
-  const uint4* g4 = reinterpret_cast<const uint4*>(g);
-  const uint4* b4 = reinterpret_cast<const uint4*>(b);
   uint4* yr = reinterpret_cast<uint4*>(y + row * 1024);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 gu = __ldg(g4 + q * 32 + lane), bu = __ldg(b4 + q * 32 + lane);
-    const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w}, bw[4] = {bu.x, bu.y, bu.z, bu.w};
+    const uint32_t gw[4] = {gu[q].x, gu[q].y, gu[q].z, gu[q].w};
+    const uint32_t bw[4] = {bu[q].x, bu[q].y, bu[q].z, bu[q].w};
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -198,7 +213,7 @@ __global__ void __launch_bounds__(128) overlay_kernel(bf16* __restrict__ hidden,
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
                      cudaStream_t stream) {
   if (M <= 0) return DS_VIT_OK;
-  layernorm_kernel<<<static_cast<unsigned>((M + 7) / 8), 256, 0, stream>>>(x, g, b, y, M, eps);
+  layernorm_kernel<<<static_cast<unsigned>((M + 3) / 4), 128, 0, stream>>>(x, g, b, y, M, eps);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 

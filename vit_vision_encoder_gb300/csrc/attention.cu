@@ -171,12 +171,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
       const uint32_t tS = tmem + x * 128, tO = tmem + kTmemO + x * 64, tP = tmem + kTmemP + x * 64;
       int consumed = 0;
+      // Descriptors are built once; a stage or K step only advances the start
+      // address field (byte offset >> 4).
+      const uint64_t dq = sdesc_sw128(sQ(x), 16, 1024);
+      const uint64_t dk0 = sdesc_sw128(sK(0), 16, 1024);
+      const uint64_t dv0 = sdesc_sw128(sV(0), kKVBytes, 1024);
       auto issue_s = [&](int j) {
-        const uint32_t k0 = sK(j % kStages);
+        const uint64_t dk = dk0 + static_cast<uint64_t>((j % kStages) * (kKVBytes >> 4));
 #pragma unroll
-        for (int k = 0; k < kHd / 16; ++k)
-          umma_bf16(tS, sdesc_sw128(sQ(x) + k * 32, 16, 1024), sdesc_sw128(k0 + k * 32, 16, 1024),
-                    id_s, k != 0);
+        for (int k = 0; k < kHd / 16; ++k) umma_bf16(tS, dq + 2 * k, dk + 2 * k, id_s, k != 0);
         umma_commit(bar(kBarSFull + x));
       };
       bool ok = mbar_wait(bar(kBarQ), 0, p.status) && mbar_wait(bar(kBarKvFull), 0, p.status);
@@ -195,11 +198,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!mbar_wait(bar(kBarPFull + x), par, p.status)) break;
         tc_fence_after();
-        const uint32_t vb = sV(j % kStages);
+        const uint64_t dv = dv0 + static_cast<uint64_t>((j % kStages) * (kKVBytes >> 4));
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k)
-          umma_bf16_ts(tO, tP + k * 8, sdesc_sw128(vb + k * 16 * 128, kKVBytes, 1024), id_o,
-                       (j | k) != 0);
+          umma_bf16_ts(tO, tP + k * 8, dv + 128 * k, id_o, (j | k) != 0);   // 16 rows = 2048 B
         umma_commit(bar(kBarPvDone + x));
         umma_commit(bar(kBarKvEmpty + j % kStages));
         consumed = j + 1;

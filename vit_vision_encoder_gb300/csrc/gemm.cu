@@ -152,6 +152,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false, false);
+      // Descriptors are built once; a stage or K step only advances the start
+      // address field (byte offset >> 4).
+      const uint64_t da0 = sdesc_sw128(stage_a(0), 16, 1024);
+      const uint64_t db0 = sdesc_sw128(stage_b(0), 16, 1024);
       int stage = 0, fills = 0;
       uint32_t phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
@@ -165,12 +169,10 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = stage_a(stage), b0 = stage_b(stage);
+          const uint64_t off = static_cast<uint64_t>(stage * (C::STAGE_BYTES >> 4));
 #pragma unroll
-          for (int k = 0; k < C::BK / 16; ++k) {
-            umma_bf16(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
-                      idesc, (kb | k) != 0);
-          }
+          for (int k = 0; k < C::BK / 16; ++k)
+            umma_bf16(d_tmem, da0 + off + 2 * k, db0 + off + 2 * k, idesc, (kb | k) != 0);
           umma_commit(empty_bar(stage));
           ++fills;
           if (++stage == C::STAGES) {

@@ -216,6 +216,57 @@ def run_reference(args):
     }), flush=True)
 
 
+def encode_flop(sizes, n_layers: int) -> int:
+    """Algorithmic FLOPs of one encode of these images (unpadded K, full
+    bidirectional attention per image)."""
+    tot = 0
+    for H, W in sizes:
+        gh, gw = H // 14, W // 14
+        n, t = gh * gw, ((gh + 2) // 3) * ((gw + 2) // 3)
+        tot += 2 * n * 1024 * 588 + 2 * t * 5120 * 9216 + 2 * t * 5120 * 5120
+        tot += n_layers * (2 * n * 1024 * (3072 + 1024 + 4096 + 4096) + 4 * n * n * 64 * 16)
+    return tot
+
+
+def other_workloads(dw, cfg, pk, reps: int = 5):
+    """images/s, merged tokens/s and the fraction of the bf16 peak on the other
+    synthetic workloads (CUDA events around the encode only)."""
+    import torch
+
+    import workloads as WL
+    import vit_vision_encoder_gb300 as dv
+    res = {}
+    for name in ("tiny", "min", "batch16", "aspect"):
+        wl = WL.WORKLOADS[name]
+        enc = dv.Encoder(dw, cfg, n_layers=wl["n_layers"])
+        imgs = [torch.from_numpy(im).cuda() for im in WL.workload_images(name)]
+        sizes = [(int(im.shape[0]), int(im.shape[1])) for im in imgs]
+        T = enc.tokens(sizes)
+        out = torch.empty((T, 5120), dtype=torch.bfloat16, device="cuda")
+        runs = wl.get("repeats", reps)
+        for _ in range(2):
+            enc.encode(imgs, out=out)
+        torch.cuda.synchronize()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(runs + 1)]
+        ev[0].record()
+        for r in range(runs):
+            enc.encode(imgs, out=out)
+            ev[r + 1].record()
+        torch.cuda.synchronize()
+        per = [ev[r].elapsed_time(ev[r + 1]) / 1e3 for r in range(runs)]
+        # the 8-run protocol of the aspect-ratio workload reports runs 2..8
+        sec = statistics.mean(per[1:] if name == "aspect" else per)
+        fl = encode_flop(sizes, wl["n_layers"])
+        res[name] = {"images": len(imgs), "layers": wl["n_layers"], "tokens": T,
+                     "ms_per_encode": round(sec * 1e3, 4), "images_per_s": round(len(imgs) / sec, 2),
+                     "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
+                     "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3)}
+        if enc.status() != dv.OK:
+            raise RuntimeError(f"device status after {name}")
+        enc.close()
+    return res
+
+
 def run_profile_case(case: str):
     """A bounded case for ncu (run it with --profile-from-start off): warm-up
     launches, then exactly the launches of interest between
@@ -266,6 +317,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-workloads", action="store_true",
+                    help="do not time the other synthetic workloads")
     ap.add_argument("--profile", default=None,
                     help="run one bounded case for ncu instead of the benchmark")
     args = ap.parse_args()
@@ -319,6 +372,7 @@ def main():
     kinds = (C.c_int32 * (per * args.steps))()
     counts = (C.c_int32 * args.steps)()
 
+    # Timed region 1 (the value): K steps, nothing else on the stream.
     clocks = ClockSampler()
     clocks.start()
     time.sleep(0.5)
@@ -328,11 +382,6 @@ def main():
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
     for s in range(args.steps):
-        ev_ptr = C.cast(C.byref(ev_arr, s * 2 * per * C.sizeof(C.c_void_p)), C.POINTER(C.c_void_p))
-        kind_ptr = C.cast(C.byref(kinds, s * per * 4), C.POINTER(C.c_int32))
-        cnt_ptr = C.cast(C.byref(counts, s * 4), C.POINTER(C.c_int32))
-        dv.check(dv.lib.ds_vit_set_kernel_timer(enc.handle, ev_ptr, kind_ptr, per, cnt_ptr),
-                 "ds_vit_set_kernel_timer")
         step()
     t1.record()
     torch.cuda.synchronize()
@@ -340,6 +389,18 @@ def main():
         dist.barrier()
     elapsed = t0.elapsed_time(t1) / 1e3
     clk = clocks.stop()
+
+    # Timed region 2 (per-kernel times, the roofline): the same K steps with CUDA
+    # events recorded around every kernel launch on the encode's stream.
+    torch.cuda.synchronize()
+    for s in range(args.steps):
+        ev_ptr = C.cast(C.byref(ev_arr, s * 2 * per * C.sizeof(C.c_void_p)), C.POINTER(C.c_void_p))
+        kind_ptr = C.cast(C.byref(kinds, s * per * 4), C.POINTER(C.c_int32))
+        cnt_ptr = C.cast(C.byref(counts, s * 4), C.POINTER(C.c_int32))
+        dv.check(dv.lib.ds_vit_set_kernel_timer(enc.handle, ev_ptr, kind_ptr, per, cnt_ptr),
+                 "ds_vit_set_kernel_timer")
+        step()
+    torch.cuda.synchronize()
     enc.detach_timer()
     status = enc.status()
     if status != dv.OK:
@@ -356,6 +417,8 @@ def main():
             d[1] += 1
             n_launch += 1
     n_launch += args.steps          # one overlay launch per step
+    n_launch //= args.steps         # launches per timed step (both regions run the same steps)
+    gpu_launches = n_launch * args.steps
 
     tmax, value = aggregate(elapsed, N_TOK * args.steps, world)
 
@@ -407,12 +470,14 @@ def main():
                      "peak_kind": f"{pk['source']} bf16 dense, sustained (kernel timed inside a long step)",
                      "flop_per_launch": KIND_FLOP["attention"], "traffic": measured_traffic()},
         "kernels": kernels,
-        "gpu_launches": n_launch,
+        "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": IMG_H * IMG_W * 3,
                 "d2h_bytes_per_step": N_TOK * 5120 * 2,
                 "api": "ds_vit_encode_batch_host (pinned pixels in, pinned embeddings out) + ds_vit_layout"},
         "clocks": clk,
     }
+    if not args.skip_workloads:
+        line["workloads"] = other_workloads(dw, cfg, pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -29,9 +29,9 @@ struct ds_vit_prepared {
   bf16* m1_perm;       // [5120, 9216], column p*1024 + c
   float* rope_cs;      // [kMaxPos, 32]
   int* status;         // device status word
-  CUtensorMap tm_patch, tm_m1, tm_m2;
-  CUtensorMap tm_qkv[DS_VIT_MAX_LAYERS], tm_proj[DS_VIT_MAX_LAYERS];
-  CUtensorMap tm_fc1[DS_VIT_MAX_LAYERS], tm_fc2[DS_VIT_MAX_LAYERS];
+  WeightMap tm_patch, tm_m1, tm_m2;
+  WeightMap tm_qkv[DS_VIT_MAX_LAYERS], tm_proj[DS_VIT_MAX_LAYERS];
+  WeightMap tm_fc1[DS_VIT_MAX_LAYERS], tm_fc2[DS_VIT_MAX_LAYERS];
   // Optional per-launch timing (ds_vit_set_kernel_timer).
   cudaEvent_t* t_events;
   int32_t* t_kinds;
@@ -319,15 +319,15 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w, ds_vit_pre
   if (rc == DS_VIT_OK) rc = launch_permute_m1(static_cast<const bf16*>(w->m1_w), p->m1_perm, 5120, st);
   if (rc == DS_VIT_OK) rc = launch_rope_table(p->rope_cs, kMaxPos, cfg->rope_theta, st);
   if (rc != DS_VIT_OK) return fail(rc);
-  bool ok = make_tmap_bf16(&p->tm_patch, p->patch_w_pad, 1024, 640, 256) &&
-            make_tmap_bf16(&p->tm_m1, p->m1_perm, 5120, 9216, 256) &&
-            make_tmap_bf16(&p->tm_m2, w->m2_w, 5120, 5120, 256);
+  bool ok = make_weight_map(&p->tm_patch, p->patch_w_pad, 1024, 640) &&
+            make_weight_map(&p->tm_m1, p->m1_perm, 5120, 9216) &&
+            make_weight_map(&p->tm_m2, w->m2_w, 5120, 5120);
   for (int l = 0; ok && l < cfg->n_layers; ++l) {
     const ds_vit_layer_weights& L = w->layers[l];
-    ok = make_tmap_bf16(&p->tm_qkv[l], L.qkv_w, 3072, 1024, 256) &&
-         make_tmap_bf16(&p->tm_proj[l], L.proj_w, 1024, 1024, 256) &&
-         make_tmap_bf16(&p->tm_fc1[l], L.fc1_w, 4096, 1024, 256) &&
-         make_tmap_bf16(&p->tm_fc2[l], L.fc2_w, 1024, 4096, 256);
+    ok = make_weight_map(&p->tm_qkv[l], L.qkv_w, 3072, 1024) &&
+         make_weight_map(&p->tm_proj[l], L.proj_w, 1024, 1024) &&
+         make_weight_map(&p->tm_fc1[l], L.fc1_w, 4096, 1024) &&
+         make_weight_map(&p->tm_fc2[l], L.fc2_w, 1024, 4096);
   }
   if (!ok) return fail(DS_VIT_ECUDA);
   if (cudaStreamSynchronize(st) != cudaSuccess) {
@@ -520,8 +520,9 @@ int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t
     return DS_VIT_EINVAL;
   if (epilogue == kEpiQkvRope && (N != 3072 || !rowpos || !rope_cs)) return DS_VIT_EINVAL;
   if (!aligned16(a) || !aligned16(w) || !aligned16(bias) || !aligned16(out)) return DS_VIT_EINVAL;
-  CUtensorMap tA, tB, tC;
-  if (!make_tmap_bf16(&tA, a, M, K, 128) || !make_tmap_bf16(&tB, w, N, K, gemm_bn(M, N)) ||
+  CUtensorMap tA, tC;
+  WeightMap tB;
+  if (!make_tmap_bf16(&tA, a, M, K, 128) || !make_weight_map(&tB, w, N, K) ||
       !make_tmap_store_bf16(&tC, out, M, N))
     return DS_VIT_ECUDA;
   return launch_gemm(tA, tB, tC, static_cast<int>(M), N, K, static_cast<const bf16*>(bias),

@@ -53,7 +53,7 @@ struct GemmCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 4;
+  static constexpr int STAGES = BN == 256 ? 4 : 6;
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 32 * 2;                // one 32x32 bf16 chunk
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;         // 2 staging chunks per warp
@@ -64,6 +64,7 @@ struct GemmCfg {
   static constexpr int THREADS = (EPI_WARPS + 2) * 32;
 };
 static_assert(GemmCfg<256>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<128>::SMEM_BYTES <= 232448, "shared memory");
 
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
@@ -404,13 +405,31 @@ bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t 
   return encode_tmap(map, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
-int gemm_bn(int /*M*/, int /*N*/) { return 256; }
+int gemm_bn(int M, int N) {
+  const int tiles256 = ((M + 127) / 128) * (N / 256);
+  return 4 * tiles256 < 3 * num_sms() ? 128 : 256;
+}
 
-int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M,
-                int N, int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
+bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k) {
+  return make_tmap_bf16(&m->bn256, w, n, k, 256) && make_tmap_bf16(&m->bn128, w, n, k, 128);
+}
+
+int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& tmC, int M, int N,
+                int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
   GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status};
+  if (gemm_bn(M, N) == 128) {
+    const CUtensorMap& tmB = B.bn128;
+    switch (epi) {
+      case kEpiBias: return launch_gemm_t<128, kEpiBias>(tmA, tmB, tmC, p, stream);
+      case kEpiBiasGelu: return launch_gemm_t<128, kEpiBiasGelu>(tmA, tmB, tmC, p, stream);
+      case kEpiBiasResid: return launch_gemm_t<128, kEpiBiasResid>(tmA, tmB, tmC, p, stream);
+      case kEpiQkvRope: return launch_gemm_t<128, kEpiQkvRope>(tmA, tmB, tmC, p, stream);
+      default: return DS_VIT_EINVAL;
+    }
+  }
+  const CUtensorMap& tmB = B.bn256;
   switch (epi) {
     case kEpiBias: return launch_gemm_t<256, kEpiBias>(tmA, tmB, tmC, p, stream);
     case kEpiBiasGelu: return launch_gemm_t<256, kEpiBiasGelu>(tmA, tmB, tmC, p, stream);

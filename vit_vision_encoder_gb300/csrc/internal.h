@@ -26,14 +26,22 @@ bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t 
 
 int num_sms();
 
-// out[M, N] = epi(A[M, K] B[N, K]^T + bias); tmB describes B with box rows == BN,
-// tmC is the store map of `out` (make_tmap_store_bf16).  Returns DS_VIT_OK or
-// DS_VIT_ECUDA.
-int launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC, int M,
-                int N, int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
+// TMA maps of one weight matrix B [N, K] for both GEMM tile widths.
+struct WeightMap {
+  CUtensorMap bn256;   // box 256 rows
+  CUtensorMap bn128;   // box 128 rows
+};
+bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k);
+
+// out[M, N] = epi(A[M, K] B[N, K]^T + bias); tmC is the store map of `out`
+// (make_tmap_store_bf16).  The tile width (gemm_bn) picks the map of B.
+// Returns DS_VIT_OK or DS_VIT_ECUDA.
+int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& tmC, int M, int N,
+                int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream);
 
-// The BN that launch_gemm uses for an N-wide output (the B tensor map's box rows).
+// Tile width: 128x256 tiles, or 128x128 when 128x256 tiles would leave more
+// than a quarter of the SMs idle (small M).
 int gemm_bn(int M, int N);
 
 // Query rows per attention CTA (two 128-row tiles).

@@ -142,6 +142,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  grid_dep_launch();
+  grid_dep_wait();
 
   __shared__ int kv_consumed[2];
   int kv_issued = 0;
@@ -362,8 +364,9 @@ int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* ou
   p.scale_log2 = 1.4426950408889634f * 0.125f;
   const int ctas = batch.tile_start[batch.n_images];
   if (ctas <= 0) return DS_VIT_OK;
-  attn_kernel<<<dim3(ctas, 16), kThreads, kSmemBytes, stream>>>(tm_qkv, p);
-  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+  const cudaError_t e = launch_pdl(attn_kernel, dim3(ctas, 16), dim3(kThreads), kSmemBytes, stream, tm_qkv, p);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 }  // namespace dsvit

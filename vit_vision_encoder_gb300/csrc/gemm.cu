@@ -120,6 +120,8 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_launch();
+  grid_dep_wait();
 
   __shared__ int consumed_fills;
   int issued_fills = 0;
@@ -351,8 +353,10 @@ int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensor
   if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
   const int tiles = ((p.M + 127) / 128) * (p.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  gemm_kernel<BN, EPI><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(tmA, tmB, tmC, p);
-  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+  const cudaError_t e =
+      launch_pdl(gemm_kernel<BN, EPI>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, tmA, tmB, tmC, p);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {

@@ -6,11 +6,32 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/dsvit.h"
 
 namespace dsvit {
 
 using bf16 = __nv_bfloat16;
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream finishes; it synchronises with
+// griddepcontrol.wait (grid_dep_wait) before touching dependent data.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Epilogue kinds of the tcgen05 GEMM (same values as DS_VIT_EPI_*).
 enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3 };

@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
                                                         float eps) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  grid_dep_launch();
+  grid_dep_wait();
   if (row >= M) return;
   // Every load of the row (x, gamma, beta) is issued before any arithmetic.
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * 1024);
@@ -100,6 +102,8 @@ __global__ void __launch_bounds__(160) im2col_kernel(const __grid_constant__ Ima
   const int gy = local / gw, gx = local % gw;
   const int W = gw * 14;
   const uint8_t* pix = batch.pix[i];
+  grid_dep_launch();
+  grid_dep_wait();
   if (threadIdx.x == 0) rowpos[n] = (gy << 16) | gx;
   uint32_t out[2];
 #pragma unroll
@@ -139,6 +143,8 @@ __global__ void __launch_bounds__(128) merge_gather_kernel(const __grid_constant
   const int w = (gw + 2) / 3;
   const int my = local / w, mx = local % w;
   uint4* dst = reinterpret_cast<uint4*>(a_m + t * 9216);
+  grid_dep_launch();
+  grid_dep_wait();
 #pragma unroll
   for (int p = 0; p < 9; ++p) {
     const int sy = 3 * my + p / 3, sx = 3 * mx + p % 3;
@@ -213,23 +219,29 @@ __global__ void __launch_bounds__(128) overlay_kernel(bf16* __restrict__ hidden,
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
                      cudaStream_t stream) {
   if (M <= 0) return DS_VIT_OK;
-  layernorm_kernel<<<static_cast<unsigned>((M + 3) / 4), 128, 0, stream>>>(x, g, b, y, M, eps);
-  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+  const cudaError_t e = launch_pdl(layernorm_kernel, dim3(static_cast<unsigned>((M + 3) / 4)), dim3(128), 0,
+                                   stream, x, g, b, y, M, eps);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 int launch_im2col(const ImageBatch& batch, const PixelNorm& norm, bf16* a_pe, int* rowpos,
                   cudaStream_t stream) {
   const int64_t rows = batch.row_off[batch.n];
   if (rows <= 0) return DS_VIT_OK;
-  im2col_kernel<<<static_cast<unsigned>(rows), 160, 0, stream>>>(batch, norm, a_pe, rowpos);
-  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+  const cudaError_t e = launch_pdl(im2col_kernel, dim3(static_cast<unsigned>(rows)), dim3(160), 0, stream,
+                                   batch, norm, a_pe, rowpos);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 int launch_merge_gather(const ImageBatch& batch, const bf16* z, bf16* a_m, cudaStream_t stream) {
   const int64_t toks = batch.tok_off[batch.n];
   if (toks <= 0) return DS_VIT_OK;
-  merge_gather_kernel<<<static_cast<unsigned>(toks), 128, 0, stream>>>(batch, z, a_m);
-  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+  const cudaError_t e =
+      launch_pdl(merge_gather_kernel, dim3(static_cast<unsigned>(toks)), dim3(128), 0, stream, batch, z, a_m);
+  if (e != cudaSuccess) cudaGetLastError();
+  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream) {

@@ -247,6 +247,21 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// ------------------------------------------------------------------ dependent launch
+
+// Let the next kernel on the stream start launching (its CTAs still wait in
+// grid_dep_wait for this grid to complete before touching its results).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding grids on the stream have completed and their memory
+// is visible.  Every kernel calls it before reading or writing data that an
+// earlier kernel produces or consumes.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ misc
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

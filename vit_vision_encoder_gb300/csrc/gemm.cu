@@ -240,17 +240,28 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
           }
         }
       }
+      // Residual: every chunk of this warp's rows is loaded before the
+      // accumulator wait, so the loads overlap the tile's main loop.
+      uint4 rxa[EPI == kEpiBiasResid ? BN / 64 : 1][4];
+      if constexpr (EPI == kEpiBiasResid) {
+#pragma unroll
+        for (int cc = 0; cc < BN / 64; ++cc) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              p.out + static_cast<size_t>(row) * p.N + nb * BN + (2 * cc + grp) * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) rxa[cc][q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
+        }
+      }
       if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
       tc_fence_after();
-#pragma unroll 1
+#pragma unroll
       for (int cc = 0; cc < BN / 64; ++cc) {
         const int c = 2 * cc + grp;
         const int n0 = nb * BN + c * 32;
         uint4 rx[4];
         if constexpr (EPI == kEpiBiasResid) {
-          const uint4* src = reinterpret_cast<const uint4*>(p.out + static_cast<size_t>(row) * p.N + n0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) rx[q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
+          for (int q = 0; q < 4; ++q) rx[q] = rxa[cc][q];
         }
         uint32_t r[32];
         tmem_ld32(tmem_base + acc * BN + c * 32 + lane_sel, r);

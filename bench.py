@@ -42,9 +42,9 @@ KIND_FLOP = {"patch_gemm": 2 * N_PATCH * 1024 * 588, "qkv_gemm": 2 * N_PATCH * 1
 ENCODE_FLOP = (KIND_FLOP["patch_gemm"] + KIND_FLOP["merger_gemm1"] + KIND_FLOP["merger_gemm2"]
                + N_LAYERS * sum(KIND_FLOP[k] for k in ("qkv_gemm", "attention", "proj_gemm",
                                                         "fc1_gemm", "fc2_gemm")))
-KIND_NAMES = ["im2col", "patch_gemm", "layernorm", "qkv_gemm", "attention", "proj_gemm",
-              "fc1_gemm", "fc2_gemm", "merge_gather", "merger_gemm1", "merger_gemm2"]
-LAUNCHES_PER_ENCODE = 1 + 1 + N_LAYERS * 7 + 1 + 1 + 2
+KIND_NAMES = ["patch_gemm", "layernorm", "qkv_gemm", "attention", "proj_gemm",
+              "fc1_gemm", "fc2_gemm", "merger_gemm1", "merger_gemm2"]
+LAUNCHES_PER_ENCODE = 1 + N_LAYERS * 7 + 1 + 2
 
 
 def peaks():

@@ -149,7 +149,8 @@ int ds_vit_workspace_bytes(const ds_vit_prepared* p, int n, const int32_t* H,
  * ds_vit_encode_batch: encode n images (n <= DS_VIT_MAX_IMAGES) packed into one
  * varlen pass; attention never crosses images.
  *   pixels: host array of n device pointers, image i is uint8 [H[i], W[i], 3]
- *           (HWC, RGB).  H[i], W[i] (host) must be positive multiples of 14;
+ *           (HWC, RGB), each 4-byte aligned (DS_VIT_EINVAL otherwise).
+ *           H[i], W[i] (host) must be positive multiples of 14;
  *           (H/14)*(W/14) <= DS_VIT_MAX_PATCHES and the merged token count
  *           ceil(H/42)*ceil(W/42) <= DS_VIT_MAX_TOKENS.
  *   out:    device bf16 [sum T_i, 5120], image i's tokens at rows
@@ -232,17 +233,17 @@ int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_s
                    void* stream);
 
 /* Kernel kinds reported by ds_vit_set_kernel_timer. */
-#define DS_VIT_KERNEL_IM2COL 0
-#define DS_VIT_KERNEL_PATCH_GEMM 1
-#define DS_VIT_KERNEL_LAYERNORM 2
-#define DS_VIT_KERNEL_QKV_GEMM 3
-#define DS_VIT_KERNEL_ATTENTION 4
-#define DS_VIT_KERNEL_PROJ_GEMM 5
-#define DS_VIT_KERNEL_FC1_GEMM 6
-#define DS_VIT_KERNEL_FC2_GEMM 7
-#define DS_VIT_KERNEL_MERGE_GATHER 8
-#define DS_VIT_KERNEL_MERGER_GEMM1 9
-#define DS_VIT_KERNEL_MERGER_GEMM2 10
+/* PATCH_GEMM patchifies and normalises the pixels inside its A-tile load;
+ * MERGER_GEMM1 gathers the 3x3 windows inside its A-tile load. */
+#define DS_VIT_KERNEL_PATCH_GEMM 0
+#define DS_VIT_KERNEL_LAYERNORM 1
+#define DS_VIT_KERNEL_QKV_GEMM 2
+#define DS_VIT_KERNEL_ATTENTION 3
+#define DS_VIT_KERNEL_PROJ_GEMM 4
+#define DS_VIT_KERNEL_FC1_GEMM 5
+#define DS_VIT_KERNEL_FC2_GEMM 6
+#define DS_VIT_KERNEL_MERGER_GEMM1 7
+#define DS_VIT_KERNEL_MERGER_GEMM2 8
 
 /*
  * ds_vit_set_kernel_timer (profiling aid): after this call, every kernel that

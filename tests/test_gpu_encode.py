@@ -111,6 +111,10 @@ def test_errors_write_nothing(dv, enc2):
     assert L.ds_vit_encode(enc2.handle, P(img), 84, 84, P(out), P(ws), 1024, st) == dv.ECAP
     assert L.ds_vit_encode(enc2.handle, P(img), 14 * 200, 14 * 200, P(out), P(ws), ws.numel(),
                            st) == dv.ERANGE
+    # Pixels must start on a 4-byte boundary (rejected before any launch).
+    padded = torch.zeros(84 * 84 * 3 + 4, dtype=torch.uint8, device="cuda")
+    assert L.ds_vit_encode(enc2.handle, C.c_void_p(padded.data_ptr() + 2), 84, 84, P(out), P(ws),
+                           ws.numel(), st) == dv.EINVAL
     torch.cuda.synchronize()
     assert bool((out == 7.0).all())
 

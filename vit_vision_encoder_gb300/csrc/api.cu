@@ -2,12 +2,14 @@
 // the sequence of kernel launches of one encode on one stream.
 //
 // Encode ("DeepSeek V4.1 Flash Engineering, Part 3: Integrating Vision"):
-//   im2col + normalise            ("Step 1" items 5-6, "Step 5")
-//   patch projection GEMM (+bias) ("Multimodal basics", second step)
+//   patch projection GEMM (+bias), its A tiles patchified and normalised
+//   in shared memory            ("Step 1" items 5-6, "Step 5";
+//                                 "Multimodal basics", second step)
 //   n_layers x [LN1, QKV GEMM (+bias, 2D RoPE), attention, out-proj GEMM
 //              (+bias, +residual), LN2, FC1 GEMM (+bias, GELU), FC2 GEMM
 //              (+bias, +residual)]   ("Step 2" table, "Step 3")
-//   final LN, 3x3 merge-gather, merger GEMM1 (+bias, GELU), GEMM2 (+bias)
+//   final LN, merger GEMM1 (+bias, GELU) with the 3x3 merge-gather done
+//   in its A producer, merger GEMM2 (+bias)
 //                                 ("Step 4", comparison table)
 // Layout and overlay: "Connect the complete image-to-text path first";
 // ds4-learning glossary "vision", V4.1 paragraph.
@@ -25,9 +27,10 @@ struct ds_vit_prepared {
   ds_vit_config cfg;
   ds_vit_weights w;
   int device;
-  bf16* patch_w_pad;   // [1024, 640]
+  bf16* patch_w_pad;   // [1024, kPatchK], patch-row-major K order
   bf16* m1_perm;       // [5120, 9216], column p*1024 + c
   float* rope_cs;      // [kMaxPos, 32]
+  bf16* pix_lut;       // [3, 256] normalised value of each (channel, byte)
   int* status;         // device status word
   WeightMap tm_patch, tm_m1, tm_m2;
   WeightMap tm_qkv[DS_VIT_MAX_LAYERS], tm_proj[DS_VIT_MAX_LAYERS];
@@ -94,7 +97,7 @@ Plan make_plan(int n, const int32_t* H, const int32_t* W, bool host_io) {
   pl.off_y = o;      o += align_up(N * 1024 * 2);
   pl.off_o = o;      o += align_up(N * 1024 * 2);
   pl.off_qkv = o;    o += align_up(std::max(N * 3072, T * 5120) * 2);
-  pl.off_h = o;      o += align_up(std::max(std::max(N * 4096, N * 640), T * 9216) * 2);
+  pl.off_h = o;      o += align_up(N * 4096 * 2);
   pl.off_rowpos = o; o += align_up(N * 4);
   if (host_io) {
     pl.off_pix = o;
@@ -173,10 +176,9 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
   bf16* h = reinterpret_cast<bf16*>(ws + pl.off_h);
   int* rowpos = reinterpret_cast<int*>(ws + pl.off_rowpos);
 
-  CUtensorMap tA_pe, tA_y, tA_o, tA_h, tA_m, tA_u, t_qkv;
-  if (!make_tmap_bf16(&tA_pe, h, N, 640, 128) || !make_tmap_bf16(&tA_y, y, N, 1024, 128) ||
-      !make_tmap_bf16(&tA_o, o, N, 1024, 128) || !make_tmap_bf16(&tA_h, h, N, 4096, 128) ||
-      !make_tmap_bf16(&tA_m, h, T, 9216, 128) || !make_tmap_bf16(&tA_u, qkv, T, 5120, 128) ||
+  CUtensorMap tA_y, tA_o, tA_h, tA_u, t_qkv;
+  if (!make_tmap_bf16(&tA_y, y, N, 1024, 128) || !make_tmap_bf16(&tA_o, o, N, 1024, 128) ||
+      !make_tmap_bf16(&tA_h, h, N, 4096, 128) || !make_tmap_bf16(&tA_u, qkv, T, 5120, 128) ||
       !make_tmap_bf16(&t_qkv, qkv, N, 3072, 128))
     return DS_VIT_ECUDA;
   CUtensorMap tC_x, tC_qkv, tC_h, tC_u, tC_out;
@@ -186,11 +188,11 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
     return DS_VIT_ECUDA;
   for (int i = 0; i <= n; ++i) tok_offsets[i] = ib.tok_off[i];
 
-  PixelNorm norm;
-  for (int c = 0; c < 3; ++c) {
-    norm.mean[c] = cfg.mean[c];
-    norm.std[c] = cfg.std[c];
-  }
+  AGenParams ag{};
+  ag.batch = ib;
+  ag.lut = p->pix_lut;
+  ag.z = y;
+  ag.rowpos = rowpos;
   // Each launch goes through `timed`, which brackets it with the caller's
   // events when a kernel timer is attached.
   int n_timed = 0;
@@ -211,10 +213,9 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
     tstop(kind);               \
     if (rc_ != DS_VIT_OK) return rc_; \
   } while (0)
-  DSV_LAUNCH(DS_VIT_KERNEL_IM2COL, launch_im2col(ib, norm, h, rowpos, st));
   DSV_LAUNCH(DS_VIT_KERNEL_PATCH_GEMM,
-             launch_gemm(tA_pe, p->tm_patch, tC_x, N, 1024, 640, static_cast<const bf16*>(w.patch_b), x,
-                         kEpiBias, nullptr, nullptr, p->status, st));
+             launch_gemm_agen(kAPixels, ag, p->tm_patch, tC_x, N, 1024, kPatchK,
+                              static_cast<const bf16*>(w.patch_b), x, kEpiBias, p->status, st));
   if (dump_blocks) DSV_CUDA(cudaMemcpyAsync(dump_blocks, x, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
   for (int l = 0; l < cfg.n_layers; ++l) {
     const ds_vit_layer_weights& L = w.layers[l];
@@ -245,10 +246,9 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
              launch_layernorm(x, static_cast<const bf16*>(w.lnm_g), static_cast<const bf16*>(w.lnm_b),
                               y, N, cfg.ln_eps, st));
   if (dump_final) DSV_CUDA(cudaMemcpyAsync(dump_final, y, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
-  DSV_LAUNCH(DS_VIT_KERNEL_MERGE_GATHER, launch_merge_gather(ib, y, h, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGER_GEMM1,
-             launch_gemm(tA_m, p->tm_m1, tC_u, T, 5120, 9216, static_cast<const bf16*>(w.m1_b), qkv,
-                         kEpiBiasGelu, nullptr, nullptr, p->status, st));
+             launch_gemm_agen(kAMerge, ag, p->tm_m1, tC_u, T, 5120, 9216,
+                              static_cast<const bf16*>(w.m1_b), qkv, kEpiBiasGelu, p->status, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGER_GEMM2,
              launch_gemm(tA_u, p->tm_m2, tC_out, T, 5120, 5120, static_cast<const bf16*>(w.m2_b), out,
                          kEpiBias, nullptr, nullptr, p->status, st));
@@ -263,7 +263,7 @@ int encode_common(const ds_vit_prepared* p, int n, const uint8_t* const* pixels,
   if (!p || !pixels || !out || !tok_offsets || !ws) return DS_VIT_EINVAL;
   DSV_TRY(check_images(n, H, W));
   for (int i = 0; i < n; ++i)
-    if (!pixels[i]) return DS_VIT_EINVAL;
+    if (!pixels[i] || (reinterpret_cast<uintptr_t>(pixels[i]) & 3) != 0) return DS_VIT_EINVAL;
   if (!aligned16(out) || !aligned16(ws) || (blocks && !aligned16(blocks)) ||
       (final_norm && !aligned16(final_norm)))
     return DS_VIT_EINVAL;
@@ -307,9 +307,10 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w, ds_vit_pre
     ds_vit_release(p);
     return rc;
   };
-  if (cudaMalloc(&p->patch_w_pad, 1024 * 640 * 2) != cudaSuccess ||
+  if (cudaMalloc(&p->patch_w_pad, 1024 * kPatchK * 2) != cudaSuccess ||
       cudaMalloc(&p->m1_perm, static_cast<size_t>(5120) * 9216 * 2) != cudaSuccess ||
       cudaMalloc(&p->rope_cs, static_cast<size_t>(kMaxPos) * 32 * 4) != cudaSuccess ||
+      cudaMalloc(&p->pix_lut, 3 * 256 * 2) != cudaSuccess ||
       cudaMalloc(&p->status, sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     return fail(DS_VIT_ENOMEM);
@@ -318,8 +319,16 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w, ds_vit_pre
   int rc = launch_pad_patch_w(static_cast<const bf16*>(w->patch_w), p->patch_w_pad, 1024, st);
   if (rc == DS_VIT_OK) rc = launch_permute_m1(static_cast<const bf16*>(w->m1_w), p->m1_perm, 5120, st);
   if (rc == DS_VIT_OK) rc = launch_rope_table(p->rope_cs, kMaxPos, cfg->rope_theta, st);
+  if (rc == DS_VIT_OK) {
+    PixelNorm norm;
+    for (int c = 0; c < 3; ++c) {
+      norm.mean[c] = cfg->mean[c];
+      norm.std[c] = cfg->std[c];
+    }
+    rc = launch_pixel_lut(norm, p->pix_lut, st);
+  }
   if (rc != DS_VIT_OK) return fail(rc);
-  bool ok = make_weight_map(&p->tm_patch, p->patch_w_pad, 1024, 640) &&
+  bool ok = make_weight_map(&p->tm_patch, p->patch_w_pad, 1024, kPatchK) &&
             make_weight_map(&p->tm_m1, p->m1_perm, 5120, 9216) &&
             make_weight_map(&p->tm_m2, w->m2_w, 5120, 5120);
   for (int l = 0; ok && l < cfg->n_layers; ++l) {
@@ -344,6 +353,7 @@ int ds_vit_release(ds_vit_prepared* p) {
   cudaFree(p->patch_w_pad);
   cudaFree(p->m1_perm);
   cudaFree(p->rope_cs);
+  cudaFree(p->pix_lut);
   cudaFree(p->status);
   delete p;
   return DS_VIT_OK;

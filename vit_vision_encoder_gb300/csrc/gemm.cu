@@ -46,35 +46,237 @@ struct GemmParams {
   int* status;
 };
 
-template <int BN>
+template <int BN, int ASRC = kATma>
 struct GemmCfg {
   static constexpr int BM = 128;
   static constexpr int BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = BN == 256 ? 4 : 6;
+  // The pixel producer's raw-byte ring and LUT take the room of one stage.
+  static constexpr int STAGES = (BN == 256 ? 4 : 6) - (ASRC == kAPixels ? 1 : 0);
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 32 * 2;                // one 32x32 bf16 chunk
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;         // 2 staging chunks per warp
   static constexpr int OFF_BIAS = OFF_STG + EPI_WARPS * 2 * STG_BYTES;
-  static constexpr int OFF_BAR = OFF_BIAS + 2 * BN * 2;        // bias, double-buffered by tile
+  // kAPixels: RAW_SLOTS pixel rows in flight per producer thread, 44 bytes
+  // (11 words: a 42-byte patch row and its 4-byte alignment) per row and slot;
+  // an odd word stride keeps the 32 rows a warp reads in distinct banks.
+  static constexpr int RAW_SLOTS = 4;
+  static constexpr int RAW_ROW = 44;
+  static constexpr int OFF_RAW = OFF_BIAS + 2 * BN * 2;        // bias, double-buffered by tile
+  static constexpr int OFF_LUT = OFF_RAW + RAW_SLOTS * BM * RAW_ROW;
+  static constexpr int OFF_BAR = ASRC == kAPixels ? OFF_LUT + 3 * 256 * 2 : OFF_RAW;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;      // + barriers + alignment slack
   static constexpr int TMEM_COLS = 2 * BN;
-  static constexpr int THREADS = (EPI_WARPS + 2) * 32;
+  // Warps 0-7 epilogue, 8 TMA, 9 MMA; with a produced A, warps 10-13 build the A
+  // tiles (one row per thread) and 14-15 idle: 16 warps keep every SM
+  // sub-partition within 4 x 32 x 128 registers.
+  static constexpr int THREADS = (ASRC == kATma ? EPI_WARPS + 2 : 16) * 32;
 };
 static_assert(GemmCfg<256>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<256, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<128, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(3 * GemmCfg<128>::STAGES + 5 <= 31, "barrier slots");
 
 __device__ __forceinline__ float gelu_erf(float x) {
   return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
 }
 
-template <int BN, int EPI>
-__global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
+// Image of packed row `row` (offsets `off`, n images) and the row's index in it.
+__device__ __forceinline__ int find_image(const int64_t* off, int n, int64_t row, int* local) {
+  int i = 0;
+  while (i + 1 < n && off[i + 1] <= row) ++i;
+  *local = static_cast<int>(row - off[i]);
+  return i;
+}
+
+// A producer, kAMerge.  A row = merged token (my, mx) of image i; column
+// p*1024 + c holds z[(3my + dy)*gw + 3mx + dx, c] with p = dy*3 + dx, or 0 where
+// the 3x3 window leaves the grid ("Step 4: The aligner pads a two-dimensional
+// grid").  A K block is one 128-byte run of one z row per A row, copied by
+// cp.async straight into the 128-byte-swizzled stage (16-byte unit u of row R
+// at unit u ^ (R & 7)); eight consecutive threads copy the eight units of one
+// row, so a warp moves four whole 128-byte lines per instruction.  Thread t
+// serves rows q*16 + t/8 (q = 0..7).  Its arrival on the stage's A barrier
+// fires once its copies have landed, so up to STAGES blocks are in flight.
+template <class C>
+__device__ __forceinline__ void produce_a_merge(const AGenParams& g, const GemmParams& p, uint8_t* smem,
+                                                uint32_t afull0, uint32_t empty0, int num_m,
+                                                int num_tiles, int num_kb, int t) {
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  const int u = t & 7;
+  for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+    // Per served row: z row of window position (0, 0), and gw << 9 | mask of
+    // the window positions inside the grid (bit p).
+    int base[8];
+    uint32_t geo[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int64_t row = static_cast<int64_t>(tile % num_m) * C::BM + q * 16 + (t >> 3);
+      base[q] = 0;
+      geo[q] = 0;
+      if (row < p.M) {
+        int local = 0;
+        const int i = find_image(g.batch.tok_off, g.batch.n, row, &local);
+        const int gh = g.batch.gh[i], gw = g.batch.gw[i];
+        const int w = (gw + 2) / 3, my = local / w, mx = local % w;
+        uint32_t mask = 0;
+#pragma unroll
+        for (int pw = 0; pw < 9; ++pw)
+          if (3 * my + pw / 3 < gh && 3 * mx + pw % 3 < gw) mask |= 1u << pw;
+        base[q] = static_cast<int>(g.batch.row_off[i]) + 3 * my * gw + 3 * mx;
+        geo[q] = (static_cast<uint32_t>(gw) << 9) | mask;
+      }
+    }
+    for (int kb = 0; kb < num_kb; ++kb) {
+      const int pw = kb >> 4, c0 = (kb & 15) * 64;
+      const int dy = pw / 3, dx = pw % 3;
+      if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status)) {
+        ok = false;
+        break;
+      }
+      const uint32_t dst0 = smem_u32(smem + stage * C::STAGE_BYTES);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int R = q * 16 + (t >> 3);
+        const bool in = (geo[q] >> pw) & 1u;
+        const int64_t zr = static_cast<int64_t>(base[q]) + dy * static_cast<int>(geo[q] >> 9) + dx;
+        const bf16* src = in ? g.z + zr * 1024 + c0 + u * 8 : g.z;
+        cp_async_16(dst0 + R * 128 + ((u ^ (R & 7)) << 4), src, in ? 16u : 0u);
+      }
+      cp_async_arrive(afull0 + 8u * stage);
+      if (++stage == C::STAGES) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+  }
+  cp_async_wait<0>();   // no copy lands after the CTA has exited
+}
+
+// Source of one patch: its top-left pixel's first byte and the image pitch.
+struct PatchSrc {
+  const uint8_t* p;
+  int pitch;            // bytes per pixel row (W * 3)
+  int gy, gx;
+  bool valid;
+};
+
+__device__ __forceinline__ PatchSrc patch_src(const AGenParams& g, int64_t row, int64_t M) {
+  PatchSrc s{g.batch.pix[0], 0, 0, 0, false};
+  if (row >= M) return s;
+  int local = 0;
+  const int i = find_image(g.batch.row_off, g.batch.n, row, &local);
+  const int gw = g.batch.gw[i];
+  s.gy = local / gw;
+  s.gx = local % gw;
+  s.pitch = gw * 14 * 3;
+  s.p = g.batch.pix[i] + static_cast<int64_t>(s.gy) * 14 * s.pitch + s.gx * 42;
+  s.valid = true;
+  return s;
+}
+
+// A producer, kAPixels ("Step 1" items 5-6, "Step 5": 14x14 patches of
+// bf16((v/255 - mean_c)/std_c)).  Thread r builds row r (one patch) of every
+// A tile; K block y holds the patch's pixel row y: its 42 bytes (x*3 + c order,
+// as they lie in the image) normalised through a per-CTA table, then 22 zero
+// columns.  The 42 bytes start on an even address (the image is 4-byte
+// aligned, rows and patches are multiples of 42 bytes apart): they are copied
+// as 11 aligned words by cp.async into a per-thread ring RAW_SLOTS rows deep,
+// so pixel loads run ahead of the conversion.
+template <class C>
+__device__ __forceinline__ void produce_a_pixels(const AGenParams& g, const GemmParams& p, uint8_t* smem,
+                                                 uint32_t afull0, uint32_t empty0, int num_m,
+                                                 int num_tiles, int r) {
+  constexpr int KB = 14;   // one patch row per K block
+  uint16_t* lut = reinterpret_cast<uint16_t*>(smem + C::OFF_LUT);
+  for (int j = r; j < 3 * 256; j += C::BM) lut[j] = reinterpret_cast<const uint16_t*>(g.lut)[j];
+  named_barrier(2, C::BM);
+  const uint32_t raw_row = smem_u32(smem + C::OFF_RAW) + r * C::RAW_ROW;
+  const int total = (num_tiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
+                    static_cast<int>(gridDim.x) * KB;
+
+  // Issue the raw copy of fill f (tile f / KB of this CTA, pixel row f % KB).
+  PatchSrc is{};
+  auto issue = [&](int f) {
+    if (f < total) {
+      const int t = f / KB, y = f % KB;
+      if (y == 0) {
+        const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+        is = patch_src(g, static_cast<int64_t>(tile % num_m) * C::BM + r, p.M);
+      }
+      const uintptr_t s = reinterpret_cast<uintptr_t>(is.p) + static_cast<uintptr_t>(y) * is.pitch;
+      const uint8_t* a = reinterpret_cast<const uint8_t*>(s & ~static_cast<uintptr_t>(3));
+      const uint32_t last = (s & 3) ? 4u : 2u;   // the run ends 2 bytes into word 10 when aligned
+      const uint32_t dst = raw_row + (f % C::RAW_SLOTS) * (C::BM * C::RAW_ROW);
+#pragma unroll
+      for (int j = 0; j < 11; ++j)
+        cp_async_4(dst + 4 * j, is.valid ? a + 4 * j : is.p, is.valid ? (j < 10 ? 4u : last) : 0u);
+    }
+    cp_async_commit();
+  };
+
+  for (int f = 0; f < C::RAW_SLOTS - 1; ++f) issue(f);
+  int stage = 0;
+  uint32_t phase = 0;
+  PatchSrc cs{};
+  for (int f = 0; f < total; ++f) {
+    issue(f + C::RAW_SLOTS - 1);
+    cp_async_wait<C::RAW_SLOTS - 1>();    // fill f's raw row has landed
+    const int t = f / KB, y = f % KB;
+    const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
+    if (y == 0) {
+      cs = patch_src(g, static_cast<int64_t>(tile % num_m) * C::BM + r, p.M);
+      if (cs.valid && tile / num_m == 0)
+        g.rowpos[static_cast<int64_t>(tile % num_m) * C::BM + r] = (cs.gy << 16) | cs.gx;
+    }
+    uint32_t w[12];
+    const uint32_t src = raw_row + (f % C::RAW_SLOTS) * (C::BM * C::RAW_ROW);
+#pragma unroll
+    for (int j = 0; j < 11; ++j) asm volatile("ld.shared.u32 %0, [%1];" : "=r"(w[j]) : "r"(src + 4 * j));
+    w[11] = 0;
+    // Start the byte sequence at the run: shift by 2 bytes when it began mid-word.
+    const bool odd_half = ((reinterpret_cast<uintptr_t>(cs.p) + static_cast<uintptr_t>(y) * cs.pitch) & 3) != 0;
+#pragma unroll
+    for (int j = 0; j < 11; ++j) w[j] = odd_half ? __funnelshift_r(w[j], w[j + 1], 16) : w[j];
+    uint32_t out[32];
+#pragma unroll
+    for (int j = 0; j < 21; ++j) {
+      const uint32_t b0 = (w[j >> 1] >> ((j & 1) * 16)) & 0xffu;
+      const uint32_t b1 = (w[j >> 1] >> ((j & 1) * 16 + 8)) & 0xffu;
+      const uint32_t v0 = lut[((2 * j) % 3) * 256 + b0];
+      const uint32_t v1 = lut[((2 * j + 1) % 3) * 256 + b1];
+      out[j] = cs.valid ? (v0 | (v1 << 16)) : 0u;
+    }
+#pragma unroll
+    for (int j = 21; j < 32; ++j) out[j] = 0u;
+    if (!mbar_wait(empty0 + 8u * stage, phase ^ 1u, p.status)) break;
+    const uint32_t dst = smem_u32(smem + stage * C::STAGE_BYTES) + r * 128;
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst + ((u ^ (r & 7)) << 4)),
+                   "r"(out[4 * u]), "r"(out[4 * u + 1]), "r"(out[4 * u + 2]), "r"(out[4 * u + 3])
+                   : "memory");
+    fence_proxy_async_smem();
+    mbar_arrive(afull0 + 8u * stage);
+    if (++stage == C::STAGES) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+  cp_async_wait<0>();   // no copy lands after the CTA has exited
+}
+
+template <int BN, int EPI, int ASRC>
+__global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using C = GemmCfg<BN>;
+                const __grid_constant__ CUtensorMap tmC, const GemmParams p,
+                const __grid_constant__ AGenParams g) {
+  using C = GemmCfg<BN, ASRC>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -86,6 +288,9 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * C::STAGES + 2 + a); };
   const uint32_t drain_bar = bar0 + 8u * (2 * C::STAGES + 4);
+  // Produced A: the stage's A tile is complete when all BM producer threads
+  // have arrived (the B tile still completes full_bar by its TMA bytes).
+  auto afull_bar = [&](int s) { return bar0 + 8u * (2 * C::STAGES + 5 + s); };
   auto stage_a = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES); };
   auto stage_b = [&](int s) { return smem_u32(smem + s * C::STAGE_BYTES + C::A_BYTES); };
 
@@ -99,6 +304,7 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      if constexpr (ASRC != kATma) mbar_init(afull_bar(s), C::BM);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -108,7 +314,7 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
     fence_barrier_init();
   }
   if (warp == 8 && lane == 0) {
-    prefetch_tensormap(&tmA);
+    if constexpr (ASRC == kATma) prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmC);
   }
@@ -139,8 +345,9 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
             ok = false;
             break;
           }
-          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
-          tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * C::BK, mb * C::BM);
+          mbar_expect_tx(full_bar(stage), ASRC == kATma ? C::STAGE_BYTES : C::B_BYTES);
+          if constexpr (ASRC == kATma)
+            tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * C::BK, mb * C::BM);
           tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
           ++issued_fills;
           if (++stage == C::STAGES) {
@@ -171,6 +378,13 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
             ok = false;
             break;
           }
+          if constexpr (ASRC != kATma) {
+            if (!mbar_wait(afull_bar(stage), phase, p.status)) {
+              ok = false;
+              break;
+            }
+            fence_proxy_async_smem();   // producer-written A -> tensor core reads
+          }
           tc_fence_after();
           const uint64_t off = static_cast<uint64_t>(stage * (C::STAGE_BYTES >> 4));
 #pragma unroll
@@ -192,6 +406,18 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
       // All MMAs of this CTA complete before TMEM is released.
       umma_commit(drain_bar);
       mbar_wait(drain_bar, 0, p.status);
+    }
+  } else if (warp >= 10) {
+    // ------------------------------------------------------------ A producers (warps 10-13)
+    if constexpr (ASRC != kATma) {
+      if constexpr (ASRC == kAMerge) {
+        if (warp < 14)
+          produce_a_merge<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_tiles, num_kb,
+                             threadIdx.x - 320);
+      } else {
+        if (warp < 14)
+          produce_a_pixels<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_tiles, threadIdx.x - 320);
+      }
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-7)
@@ -351,21 +577,22 @@ __global__ void __launch_bounds__(GemmCfg<BN>::THREADS, 1)
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, int ASRC = kATma>
 int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                  const GemmParams& p, cudaStream_t stream) {
-  using C = GemmCfg<BN>;
+                  const GemmParams& p, cudaStream_t stream, const AGenParams* g = nullptr) {
+  using C = GemmCfg<BN, ASRC>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI>,
+    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI, ASRC>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   });
   if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
   const int tiles = ((p.M + 127) / 128) * (p.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
-  const cudaError_t e =
-      launch_pdl(gemm_kernel<BN, EPI>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, stream, tmA, tmB, tmC, p);
+  static const AGenParams none{};
+  const cudaError_t e = launch_pdl(gemm_kernel<BN, EPI, ASRC>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES,
+                                   stream, tmA, tmB, tmC, p, g ? *g : none);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
@@ -452,6 +679,23 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
     case kEpiQkvRope: return launch_gemm_t<256, kEpiQkvRope>(tmA, tmB, tmC, p, stream);
     default: return DS_VIT_EINVAL;
   }
+}
+
+int launch_gemm_agen(int asrc, const AGenParams& g, const WeightMap& B, const CUtensorMap& tmC,
+                     int M, int N, int K, const bf16* bias, bf16* out, int epi, int* status,
+                     cudaStream_t stream) {
+  if (M <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
+  if (!(asrc == kAPixels && K == kPatchK && epi == kEpiBias) &&
+      !(asrc == kAMerge && K == 9216 && epi == kEpiBiasGelu))
+    return DS_VIT_EINVAL;
+  GemmParams p{M, N, K, out, bias, nullptr, nullptr, status};
+  const bool narrow = gemm_bn(M, N) == 128;
+  const CUtensorMap& tmB = narrow ? B.bn128 : B.bn256;
+  if (asrc == kAPixels)
+    return narrow ? launch_gemm_t<128, kEpiBias, kAPixels>(tmB, tmB, tmC, p, stream, &g)
+                  : launch_gemm_t<256, kEpiBias, kAPixels>(tmB, tmB, tmC, p, stream, &g);
+  return narrow ? launch_gemm_t<128, kEpiBiasGelu, kAMerge>(tmB, tmB, tmC, p, stream, &g)
+                : launch_gemm_t<256, kEpiBiasGelu, kAMerge>(tmB, tmB, tmC, p, stream, &g);
 }
 
 }  // namespace dsvit

@@ -95,21 +95,43 @@ struct PixelNorm {
   float std[3];
 };
 
-// Patchify + normalise into A_pe [sum N, 640] (columns 588..639 zero) and the
-// per-row position word gy << 16 | gx.
-int launch_im2col(const ImageBatch& batch, const PixelNorm& norm, bf16* a_pe, int* rowpos,
-                  cudaStream_t stream);
+// lut[c * 256 + v] = bf16((v/255 - mean_c)/std_c), fp32 arithmetic (3 x 256 entries).
+int launch_pixel_lut(const PixelNorm& norm, bf16* lut, cudaStream_t stream);
 
-// Gather z [sum N, 1024] into the merger input [sum T, 9216] with column
-// p*1024 + c (p = dy*3 + dx), zero where the 3x3 window leaves the grid.
-int launch_merge_gather(const ImageBatch& batch, const bf16* z, bf16* a_m, cudaStream_t stream);
+// The patch projection's K order inside the GEMM: patch row y fills columns
+// y*64 .. y*64+41 in pixel order (x*3 + c), columns y*64+42 .. y*64+63 are
+// zero.  The weight is permuted to match once at preparation; the product is
+// the same sum as over the pages' c*196 + y*14 + x order.
+constexpr int kPatchK = 14 * 64;
+
+// Where a fused GEMM's A tile comes from.
+enum ASource : int {
+  kATma = 0,      // TMA from a row-major bf16 matrix
+  kAPixels = 1,   // patchify + normalise (K = kPatchK, one patch row per 64 columns)
+  kAMerge = 2     // 3x3 merge-gather of the final-norm output, column p*1024 + c
+};
+
+struct AGenParams {
+  ImageBatch batch;
+  const bf16* lut;   // kAPixels: normalised pixel values [3][256]
+  const bf16* z;     // kAMerge: final-norm output [sum N, 1024]
+  int* rowpos;       // kAPixels writes gy << 16 | gx of every patch row here
+};
+
+// launch_gemm with the A tile built in shared memory by producer warps
+// (asrc = kAPixels: M = sum N patches, K = kPatchK; kAMerge: M = sum T tokens, K = 9216).
+// kAPixels needs every image's pixel pointer 4-byte aligned.
+int launch_gemm_agen(int asrc, const AGenParams& g, const WeightMap& B, const CUtensorMap& tmC,
+                     int M, int N, int K, const bf16* bias, bf16* out, int epi, int* status,
+                     cudaStream_t stream);
 
 int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream);
 
 // W'[o, p*1024 + c] = W[o, c*9 + p]  (rows of 9216).
 int launch_permute_m1(const bf16* w, bf16* w_perm, int rows, cudaStream_t stream);
 
-// W'[o, k] = k < 588 ? W[o, k] : 0  (rows of 640).
+// W'[o, y*64 + x*3 + c] = W[o, c*196 + y*14 + x] for x < 14, zero in columns
+// y*64 + 42 .. y*64 + 63  (rows of kPatchK).
 int launch_pad_patch_w(const bf16* w, bf16* w_pad, int rows, cudaStream_t stream);
 
 struct OverlaySpans {

@@ -1,6 +1,5 @@
-// Memory-bound kernels of the encode: LayerNorm, patchify + normalise
-// (im2col), the 3x3 merge-gather, the RoPE table, weight preparation and the
-// overlay scatter.  Sources: "DeepSeek V4.1 Flash Engineering, Part 3:
+// Memory-bound kernels of the encode: LayerNorm, the pixel normalisation
+// table, the RoPE table, weight preparation and the overlay scatter.  Sources: "DeepSeek V4.1 Flash Engineering, Part 3:
 // Integrating Vision" (cited per kernel).
 #include "internal.h"
 #include "ptx.cuh"
@@ -85,76 +84,16 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   }
 }
 
-// ---------------------------------------------------------------- patchify
-// Row n of image i = patch (gy, gx) = (n / gw, n % gw); column k = c*196 +
-// y*14 + x holds pixel (gy*14 + y, gx*14 + x, c) mapped to
-// bf16((p/255 - mean_c)/std_c) ("Step 1", items 5 and 6; "Step 5": 588
-// columns, here padded with zeros to 640 for 64-wide K tiles).
-// One block of 160 threads per patch row; thread t writes 4 columns.
-__global__ void __launch_bounds__(160) im2col_kernel(const __grid_constant__ ImageBatch batch,
-                                                     const __grid_constant__ PixelNorm norm,
-                                                     bf16* __restrict__ a_pe, int* __restrict__ rowpos) {
-  const int64_t n = blockIdx.x;
-  int i = 0;
-  while (i + 1 < batch.n && batch.row_off[i + 1] <= n) ++i;
-  const int local = static_cast<int>(n - batch.row_off[i]);
-  const int gw = batch.gw[i];
-  const int gy = local / gw, gx = local % gw;
-  const int W = gw * 14;
-  const uint8_t* pix = batch.pix[i];
-  grid_dep_launch();
-  grid_dep_wait();
-  if (threadIdx.x == 0) rowpos[n] = (gy << 16) | gx;
-  uint32_t out[2];
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float f[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int k = threadIdx.x * 4 + h * 2 + e;
-      float val = 0.f;
-      if (k < 588) {
-        const int c = k / 196, rem = k % 196, y = rem / 14, x = rem % 14;
-        const float p = static_cast<float>(pix[(static_cast<int64_t>(gy * 14 + y) * W + gx * 14 + x) * 3 + c]);
-        val = __fdiv_rn(__fsub_rn(__fdiv_rn(p, 255.f), norm.mean[c]), norm.std[c]);
-      }
-      f[e] = val;
-    }
-    out[h] = pack_bf16x2(f[0], f[1]);
-  }
-  *reinterpret_cast<uint2*>(a_pe + n * 640 + threadIdx.x * 4) = make_uint2(out[0], out[1]);
-}
-
-// ---------------------------------------------------------------- merge-gather
-// Merged token t = my*w + mx of image i, window position p = dy*3 + dx:
-// A[t, p*1024 + c] = z[(3my+dy)*gw + 3mx+dx, c], or 0 when (3my+dy, 3mx+dx)
-// falls in the right/bottom padding ("Step 4: The aligner pads a
-// two-dimensional grid").  The position-major column order matches the
-// merger weight permuted at preparation (same sum as the channel-major unfold).
-// Block = one merged token, 9 x 128 threads of 16 bytes.
-__global__ void __launch_bounds__(128) merge_gather_kernel(const __grid_constant__ ImageBatch batch,
-                                                           const bf16* __restrict__ z,
-                                                           bf16* __restrict__ a_m) {
-  const int64_t t = blockIdx.x;
-  int i = 0;
-  while (i + 1 < batch.n && batch.tok_off[i + 1] <= t) ++i;
-  const int local = static_cast<int>(t - batch.tok_off[i]);
-  const int gh = batch.gh[i], gw = batch.gw[i];
-  const int w = (gw + 2) / 3;
-  const int my = local / w, mx = local % w;
-  uint4* dst = reinterpret_cast<uint4*>(a_m + t * 9216);
-  grid_dep_launch();
-  grid_dep_wait();
-#pragma unroll
-  for (int p = 0; p < 9; ++p) {
-    const int sy = 3 * my + p / 3, sx = 3 * mx + p % 3;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (sy < gh && sx < gw) {
-      const uint4* src = reinterpret_cast<const uint4*>(z + (batch.row_off[i] + sy * gw + sx) * 1024);
-      v = src[threadIdx.x];
-    }
-    dst[p * 128 + threadIdx.x] = v;
-  }
+// ---------------------------------------------------------------- pixel LUT
+// lut[c*256 + v] = bf16((v/255 - mean_c)/std_c) in fp32 arithmetic ("Step 1"
+// item 6 with the CLIP statistics); the patch-projection GEMM reads it while
+// building its A tiles.
+__global__ void pixel_lut_kernel(const __grid_constant__ PixelNorm norm, bf16* __restrict__ lut) {
+  const int t = threadIdx.x + blockIdx.x * blockDim.x;
+  if (t >= 768) return;
+  const int c = t / 256, v = t % 256;
+  lut[t] = __float2bfloat16_rn(__fdiv_rn(__fsub_rn(__fdiv_rn(static_cast<float>(v), 255.f), norm.mean[c]),
+                                         norm.std[c]));
 }
 
 // ---------------------------------------------------------------- RoPE table
@@ -180,8 +119,10 @@ __global__ void permute_m1_kernel(const bf16* __restrict__ w, bf16* __restrict__
 
 __global__ void pad_patch_w_kernel(const bf16* __restrict__ w, bf16* __restrict__ wp) {
   const int64_t o = blockIdx.x;
-  for (int k = threadIdx.x; k < 640; k += blockDim.x)
-    wp[o * 640 + k] = k < 588 ? w[o * 588 + k] : __float2bfloat16_rn(0.f);
+  for (int k = threadIdx.x; k < kPatchK; k += blockDim.x) {
+    const int y = k / 64, j = k % 64, x = j / 3, c = j % 3;
+    wp[o * kPatchK + k] = j < 42 ? w[o * 588 + c * 196 + y * 14 + x] : __float2bfloat16_rn(0.f);
+  }
 }
 
 // ---------------------------------------------------------------- overlay
@@ -225,23 +166,9 @@ int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
-int launch_im2col(const ImageBatch& batch, const PixelNorm& norm, bf16* a_pe, int* rowpos,
-                  cudaStream_t stream) {
-  const int64_t rows = batch.row_off[batch.n];
-  if (rows <= 0) return DS_VIT_OK;
-  const cudaError_t e = launch_pdl(im2col_kernel, dim3(static_cast<unsigned>(rows)), dim3(160), 0, stream,
-                                   batch, norm, a_pe, rowpos);
-  if (e != cudaSuccess) cudaGetLastError();
-  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
-}
-
-int launch_merge_gather(const ImageBatch& batch, const bf16* z, bf16* a_m, cudaStream_t stream) {
-  const int64_t toks = batch.tok_off[batch.n];
-  if (toks <= 0) return DS_VIT_OK;
-  const cudaError_t e =
-      launch_pdl(merge_gather_kernel, dim3(static_cast<unsigned>(toks)), dim3(128), 0, stream, batch, z, a_m);
-  if (e != cudaSuccess) cudaGetLastError();
-  return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+int launch_pixel_lut(const PixelNorm& norm, bf16* lut, cudaStream_t stream) {
+  pixel_lut_kernel<<<3, 256, 0, stream>>>(norm, lut);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
 int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream) {

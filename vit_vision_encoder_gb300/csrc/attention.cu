@@ -8,15 +8,23 @@
 // glossary "vision", family table).
 //
 // One CTA = one (image, 256 query rows, head), as two 128-row query tiles A
-// and B that share every K/V tile.  Warps 0-3 run the softmax of tile A and
-// warps 4-7 that of tile B (one query row per thread, TMEM lane = row); warp 8
-// loads Q once and streams K/V tiles of 128 rows through a 4-stage TMA ring;
-// warp 9 issues the MMAs of tile A and warp 10 those of tile B, so the two
-// tiles proceed independently on the tensor core:
+// and B that share every K/V tile.  Warps 0-7 run the softmax of tile A and
+// warps 8-15 that of tile B: two threads per query row (TMEM lane = row), one
+// per 64-key half of the score tile, which exchange their half-row maxima
+// through shared memory (an mbarrier per lane quadrant), so every SM
+// sub-partition runs four softmax warps.  Warp 16 loads Q once and streams K/V
+// tiles of 128 rows through a 4-stage TMA ring; warp 17 issues the MMAs of
+// tile A and warp 18 those of tile B, so the two tiles proceed independently
+// on the tensor core:
 //   S_X = Q_X K_j^T     (M 128, N 128, K 64)  smem x smem -> TMEM
 //   O_X += P_X V_j      (M 128, N 64,  K 128) TMEM x smem -> TMEM
-// A softmax warpgroup reads S_X from TMEM and hands the buffer back at once,
-// so the next S_X is computed while it works.  The running row maximum m
+// The softmax threads of a tile read S_X from TMEM and hand the buffer back at
+// once, so the next S_X is computed while they work.  The exponent math of the
+// two tiles takes turns (A of step j, B of step j, A of step j+1, ...: an
+// mbarrier per tile), so each sub-partition runs one tile's math at full issue
+// rate while the tensor core works on the other tile; left to run together the
+// two tiles fall into step and their math serialises with the MMAs (1.5x
+// slower).  The running row maximum m
 // (exp2 domain) is raised only when a tile's maximum exceeds it by more than
 // 8, so P = exp2(s - m) stays below 2^8 and O is rescaled (in TMEM, by
 // exp2(m_old - m_new)) rarely; the final O / l uses the same m, so the result
@@ -46,7 +54,9 @@ constexpr int kSmemBytes = kOffBar + 256 + 1024;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;
 constexpr uint32_t kTmemP = 384;
-constexpr int kThreads = 352;         // 8 softmax warps, TMA warp, 2 MMA warps
+constexpr int kThreads = 608;         // 16 softmax warps, TMA warp, 2 MMA warps
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;          // 17: tile A, 18: tile B
 constexpr float kRescaleThreshold = 8.f;   // log2 units: P stays below 2^8
 
 // Barrier slots (8 bytes each).
@@ -57,7 +67,9 @@ enum : int {
   kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
   kBarDrain = kBarPvDone + 2,          // [2]
-  kBarCount = kBarDrain + 2
+  kBarXch = kBarDrain + 2,             // [2 tiles][4 quadrants]: half-row exchange
+  kBarTurn = kBarXch + 8,              // [2]: tile X finished the math of a step
+  kBarCount = kBarTurn + 2
 };
 static_assert(kBarCount <= 30, "barrier area");
 
@@ -92,9 +104,10 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return r;
 }
 
-// Registers are split per SM sub-partition: with 11 warps three of them share
-// one sub-partition's 16K registers, which caps a thread at 168.
-__global__ void __launch_bounds__(kThreads, 1)
+// Registers are split per SM sub-partition: with 19 warps five of them share
+// one sub-partition's 16K registers, which caps a thread at 96 (allocation in
+// units of 8).
+__global__ void __maxnreg__(96)
     attn_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ AttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -126,15 +139,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(kBarSFull + x), 1);
-      mbar_init(bar(kBarSFree + x), 128);
-      mbar_init(bar(kBarPFull + x), 128);
+      mbar_init(bar(kBarSFree + x), 256);
+      mbar_init(bar(kBarPFull + x), 256);
       mbar_init(bar(kBarPvDone + x), 1);
       mbar_init(bar(kBarDrain + x), 1);
+      for (int q = 0; q < 4; ++q) mbar_init(bar(kBarXch + 4 * x + q), 64);
+      mbar_init(bar(kBarTurn + x), 256);
     }
     fence_barrier_init();
   }
-  if (warp == 8 && lane == 0) prefetch_tensormap(&tm);
-  if (warp == 9) {
+  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tm);
+  if (warp == kWarpTma) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -146,10 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();
 
   __shared__ int kv_consumed[2];
+  // Half-row values exchanged between the two threads of a row:
+  // [exchange parity][tile][half][row].
+  __shared__ float xch[2][2][2][kTile];
   int kv_issued = 0;
   bool q_issued = false;
 
-  if (warp == 8) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       mbar_expect_tx(bar(kBarQ), 2 * kQBytes);
@@ -165,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++kv_issued;
       }
     }
-  } else if (warp >= 9) {
+  } else if (warp >= kWarpMma) {
     // ------------------------------------------------------------ MMA issuer of tile X
-    const int x = warp - 9;
+    const int x = warp - kWarpMma;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
       constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
@@ -214,13 +232,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(bar(kBarDrain + x), 0, p.status);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
-    const int x = warp >> 2;                 // query tile A (0) or B (1)
-    const int r = threadIdx.x & 127;         // row inside the tile == TMEM lane
-    const uint32_t lane_sel = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + lane_sel;
-    const uint32_t tO = tmem + kTmemO + x * 64 + lane_sel;
-    const uint32_t tP = tmem + kTmemP + x * 64 + lane_sel;
+    // ------------------------------------------------------------ softmax (warps 0-15)
+    const int x = warp >> 3;                 // query tile A (0) or B (1)
+    const int qd = warp & 3;                 // TMEM lane quadrant
+    const int h = (warp >> 2) & 1;           // 64-key half of the score tile
+    const int r = qd * 32 + lane;            // row inside the tile == TMEM lane
+    const uint32_t lane_sel = static_cast<uint32_t>(qd * 32) << 16;
+    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;
+    const uint32_t tO = tmem + kTmemO + x * 64 + h * 32 + lane_sel;
+    const uint32_t tP = tmem + kTmemP + x * 64 + h * 32 + lane_sel;
+    const uint32_t xbar = bar(kBarXch + 4 * x + qd);
+    // Both threads of a row write their half's value, arrive, wait for the
+    // phase and read the other's; slot parity e alternates, so a slot is
+    // rewritten only after its reader has arrived at the next exchange.
+    auto exchange = [&](float v, int e, float* other) {
+      xch[e & 1][x][h][r] = v;
+      mbar_arrive(xbar);
+      if (!mbar_wait(xbar, e & 1, p.status)) return false;
+      *other = xch[e & 1][x][h ^ 1][r];
+      return true;
+    };
     const float c = p.scale_log2;
     const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
@@ -232,22 +263,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        tmem_ld32(tS + q * 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32 * q));
+      uint32_t sr[64];
+      tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
-      const int kv_valid = len - j * kTile;
-      if (kv_valid < kTile) {
+      // Take turns: A's step j after B's step j-1, B's step j after A's step j.
+      if (x == 1 || j > 0) {
+        if (!mbar_wait(bar(kBarTurn + (x ^ 1)), (x == 1 ? j : j - 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
+      }
+      const int kv_valid = len - j * kTile - h * 64;
+      if (kv_valid < 64) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i >= kv_valid) sr[i] = __float_as_uint(-INFINITY);
       }
-      float mx[8];
+      float mx[4];
 #pragma unroll
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < 4; ++g) {
         const uint32_t* v = sr + 16 * g;
         float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
         a = max3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
@@ -258,8 +295,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         a = max3(a, __uint_as_float(v[13]), __uint_as_float(v[14]));
         mx[g] = fmaxf(a, __uint_as_float(v[15]));
       }
-      const float m_tile =
-          max3(max3(mx[0], mx[1], mx[2]), max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * c;
+      const float m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
+      float m_other;
+      if (!exchange(m_half, j, &m_other)) {
+        ok = false;
+        break;
+      }
+      // Both threads of the row derive the same m_new and alpha.
+      const float m_tile = fmaxf(m_half, m_other) * c;
       float m_new = m, alpha = 1.f;
       if (m_tile > m + kRescaleThreshold) {   // always true on the first tile (m = -inf)
         m_new = m_tile;
@@ -267,9 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const uint64_t nm2 = f2(-m_new, -m_new);
       uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
+      for (int i = 0; i < 32; ++i) {
         const uint64_t t = f2_fma(f2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nm2);
         float t0, t1;
         f2_split(t, t0, t1);
@@ -277,10 +320,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
+      mbar_arrive(bar(kBarTurn + x));         // the other tile's turn
       const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float s0, s1;
       f2_split(s2, s0, s1);
-      l = l * alpha + (s0 + s1);
+      l = l * alpha + (s0 + s1);              // this half's share of the row sum
       if (j > 0) {
         // PV_X of the previous tile must be done: it read P_X, and O_X is rescaled below.
         if (!mbar_wait(bar(kBarPvDone + x), par ^ 1, p.status)) {
@@ -289,36 +333,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
       }
-      tmem_st32(tP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
-      tmem_st32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+      tmem_st32(tP, pk);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        uint32_t o[32];
+        tmem_ld32(tO, o);
+        tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tO + q * 32, o);
-          tmem_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + q * 32, o);
-        }
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO, o);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + x));
       m = m_new;
     }
-    if (ok && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
+    float l_other = 0.f;
+    if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
-      const float inv_l = 1.f / l;
-      uint32_t o[64];
-      tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
-      tmem_ld32(tO + 32, *reinterpret_cast<uint32_t(*)[32]>(o + 32));
+      const float inv_l = 1.f / (l + l_other);
+      uint32_t o[32];
+      tmem_ld32(tO, o);
       tmem_wait_ld();
       const int qrow = q0 + x * kTile + r;
       if (qrow < row0 + len) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * 1024 + head * kHd);
+        uint4* dst =
+            reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * 1024 + head * kHd + h * 32);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int q = 0; q < 4; ++q) {
           dst[q] = make_uint4(
               pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l),
               pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l),
@@ -331,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8 && lane == 0 && status_failed(p.status)) {
+  if (warp == kWarpTma && lane == 0 && status_failed(p.status)) {
     // After a timeout: wait (bounded) for the loads still in flight, so no TMA
     // write lands in shared memory after the CTA has exited.
     if (q_issued) mbar_wait(bar(kBarQ), 0, nullptr);
@@ -340,7 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!mbar_wait(bar(kBarKvFull + j % kStages), (j / kStages) & 1, nullptr)) break;
   }
   __syncthreads();
-  if (warp == 9) {
+  if (warp == kWarpTma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

@@ -81,6 +81,35 @@ def test_linear_epilogues(dv, M, K, N, epi):
     assert (got == ref).mean() > 0.98
 
 
+def test_gelu_epilogue_every_bf16_input(dv):
+    """Every bf16 value in [-10, 10] passes through the GELU epilogue unchanged
+    by the product (one-hot A column times unit weights), so the output is
+    bf16(GELU(x)) of the kernel's erf evaluation: it must equal the oracle's
+    float64 erf rounded to bf16, up to one ulp where the exact value lies
+    within the approximation error of a rounding boundary.  Below x = -8.3
+    the oracle's 1 + erf cancels to 0 in float64 while the kernel keeps the
+    tail (about 1e-16): those compare by absolute difference."""
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    vals = O.bits_to_f32(bits)
+    keep = np.isfinite(vals) & (np.abs(vals) <= 10.0)
+    bits, vals = bits[keep], vals[keep]
+    M = len(bits)
+    a = np.zeros((M, 64), dtype=np.uint16)
+    a[:, 0] = bits
+    w = np.zeros((256, 64), dtype=np.uint16)
+    w[:, 0] = WL.to_bf16_bits(np.ones(256, dtype=np.float32))
+    b = np.zeros(256, dtype=np.uint16)
+    y, st = dv.op_linear(dev(a, torch), dev(w, torch), dev(b, torch), dv.EPI_BIAS_GELU)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    got = O.f32_to_bits(host(y)).astype(np.int32)
+    ref = O.f32_to_bits(O.round_bf16(O.gelu(vals))).astype(np.int32)
+    ulps = np.abs(got - ref[:, None])
+    tiny = np.abs(host(y) - O.round_bf16(O.gelu(vals))[:, None]) <= 1e-6
+    assert ulps[~tiny].max() <= 1, f"max {ulps[~tiny].max()} ulp"
+    assert (ulps == 0).mean() > 0.995
+
+
 @pytest.mark.parametrize("gh,gw", [(6, 6), (25, 21), (192, 2)])
 def test_linear_qkv_rope(dv, gh, gw):
     M = gh * gw

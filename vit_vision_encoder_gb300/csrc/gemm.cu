@@ -44,7 +44,12 @@ struct GemmParams {
   const int* rowpos;
   const float* rope_cs;
   int* status;
+  int n_fast;         // tile order: 1 = n-block fastest, 0 = m-block fastest
 };
+
+// n-block-fastest order when the A operand would not stay in L2 between the
+// passes over its n-blocks.
+int tile_order(int64_t M, int K) { return M * K * 2 > (int64_t{40} << 20) ? 1 : 0; }
 
 template <int BN, int ASRC = kATma>
 struct GemmCfg {
@@ -80,8 +85,73 @@ static_assert(GemmCfg<256, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(3 * GemmCfg<128>::STAGES + 5 <= 31, "barrier slots");
 
-__device__ __forceinline__ float gelu_erf(float x) {
-  return 0.5f * x * (1.0f + erff(x * 0.70710678118654752f));
+// GELU(x) = x Phi(x), Phi from erf ("End-to-end results and their limits":
+// the erf form).  erf by Abramowitz & Stegun 7.1.26 (Hastings): for z >= 0,
+// erfc(z) ~ q = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) with
+// t = 1 / (1 + p z), |erf error| <= 1.5e-7; then 2 Phi(x) = 2 - q for x >= 0
+// and q for x < 0 (z = |x| / sqrt 2), so the negative tail keeps its relative
+// precision.  Over [-10, 10] the GELU error is below 2.2e-7 absolute and
+// 1.7e-4 relative wherever |GELU| > 1e-3.  Two elements per call, on packed
+// f32x2 arithmetic; reciprocal and exp2 are the MUFU approximations.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ void gelu_erf2(float& x0, float& x1) {
+  const float kP = 0.3275911f;
+  const uint64_t a5 = pk2(1.061405429f, 1.061405429f), a4 = pk2(-1.453152027f, -1.453152027f);
+  const uint64_t a3 = pk2(1.421413741f, 1.421413741f), a2 = pk2(-0.284496736f, -0.284496736f);
+  const uint64_t a1 = pk2(0.254829592f, 0.254829592f);
+  const float z0 = fabsf(x0) * 0.70710678118654752f, z1 = fabsf(x1) * 0.70710678118654752f;
+  const uint64_t z = pk2(z0, z1);
+  float d0, d1;
+  upk2(fma2(pk2(kP, kP), z, pk2(1.f, 1.f)), d0, d1);
+  const uint64_t t = pk2(rcp_approx(d0), rcp_approx(d1));
+  uint64_t poly = fma2(a5, t, a4);
+  poly = fma2(poly, t, a3);
+  poly = fma2(poly, t, a2);
+  poly = fma2(poly, t, a1);
+  poly = mul2(poly, t);
+  float w0, w1;   // -z^2 log2(e)
+  upk2(mul2(mul2(z, z), pk2(-1.4426950408889634f, -1.4426950408889634f)), w0, w1);
+  float q0, q1;
+  upk2(mul2(poly, pk2(ex2_approx(w0), ex2_approx(w1))), q0, q1);
+  const float p0 = x0 >= 0.f ? 2.f - q0 : q0, p1 = x1 >= 0.f ? 2.f - q1 : q1;   // 2 Phi
+  float g0, g1;
+  upk2(mul2(mul2(pk2(x0, x1), pk2(0.5f, 0.5f)), pk2(p0, p1)), g0, g1);
+  x0 = g0;
+  x1 = g1;
+}
+
+// Tile order.  n-block fastest: the CTAs resident at one time cover few row
+// blocks of A, each read from DRAM once and shared through L2 by all the
+// n-blocks of its row (m-block-fastest order re-read the 75 MB A of the FC2
+// shape from DRAM once per n-block column).  m-block fastest: the resident
+// CTAs share few B tiles, which suits an A that stays in L2 anyway.
+__device__ __forceinline__ int tile_mb(int tile, int num_m, int num_n, int n_fast) {
+  return n_fast ? tile / num_n : tile % num_m;
+}
+__device__ __forceinline__ int tile_nb(int tile, int num_m, int num_n, int n_fast) {
+  return n_fast ? tile % num_n : tile / num_m;
 }
 
 // Image of packed row `row` (offsets `off`, n images) and the row's index in it.
@@ -104,7 +174,7 @@ __device__ __forceinline__ int find_image(const int64_t* off, int n, int64_t row
 template <class C>
 __device__ __forceinline__ void produce_a_merge(const AGenParams& g, const GemmParams& p, uint8_t* smem,
                                                 uint32_t afull0, uint32_t empty0, int num_m,
-                                                int num_tiles, int num_kb, int t) {
+                                                int num_n, int num_tiles, int num_kb, int t) {
   int stage = 0;
   uint32_t phase = 0;
   bool ok = true;
@@ -115,8 +185,9 @@ __device__ __forceinline__ void produce_a_merge(const AGenParams& g, const GemmP
     int base[8];
     uint32_t geo[8];
 #pragma unroll
+    const int64_t row0 = static_cast<int64_t>(tile_mb(tile, num_m, num_n, p.n_fast)) * C::BM;
     for (int q = 0; q < 8; ++q) {
-      const int64_t row = static_cast<int64_t>(tile % num_m) * C::BM + q * 16 + (t >> 3);
+      const int64_t row = row0 + q * 16 + (t >> 3);
       base[q] = 0;
       geo[q] = 0;
       if (row < p.M) {
@@ -191,7 +262,7 @@ __device__ __forceinline__ PatchSrc patch_src(const AGenParams& g, int64_t row, 
 template <class C>
 __device__ __forceinline__ void produce_a_pixels(const AGenParams& g, const GemmParams& p, uint8_t* smem,
                                                  uint32_t afull0, uint32_t empty0, int num_m,
-                                                 int num_tiles, int r) {
+                                                 int num_n, int num_tiles, int r) {
   constexpr int KB = 14;   // one patch row per K block
   uint16_t* lut = reinterpret_cast<uint16_t*>(smem + C::OFF_LUT);
   for (int j = r; j < 3 * 256; j += C::BM) lut[j] = reinterpret_cast<const uint16_t*>(g.lut)[j];
@@ -207,7 +278,8 @@ __device__ __forceinline__ void produce_a_pixels(const AGenParams& g, const Gemm
       const int t = f / KB, y = f % KB;
       if (y == 0) {
         const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
-        is = patch_src(g, static_cast<int64_t>(tile % num_m) * C::BM + r, p.M);
+        const int64_t row = static_cast<int64_t>(tile_mb(tile, num_m, num_n, p.n_fast)) * C::BM + r;
+        is = patch_src(g, row, p.M);
       }
       const uintptr_t s = reinterpret_cast<uintptr_t>(is.p) + static_cast<uintptr_t>(y) * is.pitch;
       const uint8_t* a = reinterpret_cast<const uint8_t*>(s & ~static_cast<uintptr_t>(3));
@@ -230,9 +302,9 @@ __device__ __forceinline__ void produce_a_pixels(const AGenParams& g, const Gemm
     const int t = f / KB, y = f % KB;
     const int tile = static_cast<int>(blockIdx.x) + t * static_cast<int>(gridDim.x);
     if (y == 0) {
-      cs = patch_src(g, static_cast<int64_t>(tile % num_m) * C::BM + r, p.M);
-      if (cs.valid && tile / num_m == 0)
-        g.rowpos[static_cast<int64_t>(tile % num_m) * C::BM + r] = (cs.gy << 16) | cs.gx;
+      const int64_t row = static_cast<int64_t>(tile_mb(tile, num_m, num_n, p.n_fast)) * C::BM + r;
+      cs = patch_src(g, row, p.M);
+      if (cs.valid && tile_nb(tile, num_m, num_n, p.n_fast) == 0) g.rowpos[row] = (cs.gy << 16) | cs.gx;
     }
     uint32_t w[12];
     const uint32_t src = raw_row + (f % C::RAW_SLOTS) * (C::BM * C::RAW_ROW);
@@ -338,7 +410,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        const int mb = tile % num_m, nb = tile / num_m;
+        const int mb = tile_mb(tile, num_m, num_n, p.n_fast), nb = tile_nb(tile, num_m, num_n, p.n_fast);
         bool ok = true;
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(empty_bar(stage), phase ^ 1u, p.status)) {
@@ -412,11 +484,12 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     if constexpr (ASRC != kATma) {
       if constexpr (ASRC == kAMerge) {
         if (warp < 14)
-          produce_a_merge<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_tiles, num_kb,
+          produce_a_merge<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_n, num_tiles, num_kb,
                              threadIdx.x - 320);
       } else {
         if (warp < 14)
-          produce_a_pixels<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_tiles, threadIdx.x - 320);
+          produce_a_pixels<C>(g, p, smem, afull_bar(0), empty_bar(0), num_m, num_n, num_tiles,
+                              threadIdx.x - 320);
       }
     }
   } else {
@@ -429,7 +502,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     uint32_t acc = 0, acc_phase = 0;
     int stg = 0, it = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int mb = tile % num_m, nb = tile / num_m;
+      const int mb = tile_mb(tile, num_m, num_n, p.n_fast), nb = tile_nb(tile, num_m, num_n, p.n_fast);
       // The tile's bias -> shared memory (buffer it & 1), by warp 0.
       const uint32_t bias_buf = bias_s + (it & 1) * (BN * 2);
       if (warp == 0) {
@@ -512,7 +585,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
         }
         if constexpr (EPI == kEpiBiasGelu) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = gelu_erf(v[i]);
+          for (int i = 0; i < 32; i += 2) gelu_erf2(v[i], v[i + 1]);
         } else if constexpr (EPI == kEpiBiasResid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -660,7 +733,7 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
                 int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
-  GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status};
+  GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status, tile_order(M, K)};
   if (gemm_bn(M, N) == 128) {
     const CUtensorMap& tmB = B.bn128;
     switch (epi) {
@@ -688,7 +761,7 @@ int launch_gemm_agen(int asrc, const AGenParams& g, const WeightMap& B, const CU
   if (!(asrc == kAPixels && K == kPatchK && epi == kEpiBias) &&
       !(asrc == kAMerge && K == 9216 && epi == kEpiBiasGelu))
     return DS_VIT_EINVAL;
-  GemmParams p{M, N, K, out, bias, nullptr, nullptr, status};
+  GemmParams p{M, N, K, out, bias, nullptr, nullptr, status, tile_order(M, K)};
   const bool narrow = gemm_bn(M, N) == 128;
   const CUtensorMap& tmB = narrow ? B.bn128 : B.bn256;
   if (asrc == kAPixels)

@@ -10,9 +10,11 @@ namespace {
 
 // ---------------------------------------------------------------- LayerNorm
 // One warp per 1024-wide row; each lane holds 32 values (four 16-byte loads,
-// coalesced across the warp).  fp32 statistics: mean, then the biased variance
-// of the centred values; y = (x - mu) * (1/sqrt(var + eps)) * g + b rounded to
-// bf16 ("Step 2": the final-norm boundary; block pre-norms).
+// coalesced across the warp), kept packed as bf16 pairs so a thread needs few
+// registers and many rows stay in flight per SM.  fp32 statistics: mean, then
+// the biased variance of the centred values; y = (x - mu) * (1/sqrt(var + eps))
+// * g + b rounded to bf16 ("Step 2": the final-norm boundary; block pre-norms).
+// gamma and beta are read after the statistics (they are hot in L1/L2).
 __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ x,
                                                         const bf16* __restrict__ g,
                                                         const bf16* __restrict__ b,
@@ -23,33 +25,21 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   grid_dep_launch();
   grid_dep_wait();
   if (row >= M) return;
-  // Every load of the row (x, gamma, beta) is issued before any arithmetic.
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * 1024);
-  const uint4* g4 = reinterpret_cast<const uint4*>(g);
-  const uint4* b4 = reinterpret_cast<const uint4*>(b);
-  uint4 xu[4], gu[4], bu[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) xu[q] = __ldg(xr + q * 32 + lane);
+  uint32_t xw[16];
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    gu[q] = __ldg(g4 + q * 32 + lane);
-    bu[q] = __ldg(b4 + q * 32 + lane);
-  }
-  float v[32];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint32_t w[4] = {xu[q].x, xu[q].y, xu[q].z, xu[q].w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      v[q * 8 + 2 * e] = bf16lo(w[e]);
-      v[q * 8 + 2 * e + 1] = bf16hi(w[e]);
-    }
+    const uint4 u = __ldg(xr + q * 32 + lane);
+    xw[4 * q] = u.x;
+    xw[4 * q + 1] = u.y;
+    xw[4 * q + 2] = u.z;
+    xw[4 * q + 3] = u.w;
   }
   float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    s0 += v[i];
-    s1 += v[i + 1];
+  for (int i = 0; i < 16; ++i) {
+    s0 += bf16lo(xw[i]);
+    s1 += bf16hi(xw[i]);
   }
   float s = s0 + s1;
 #pragma unroll
@@ -57,27 +47,31 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   const float mu = __fdiv_rn(s, 1024.f);
   float q0 = 0.f, q1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    v[i] = __fsub_rn(v[i], mu);
-    v[i + 1] = __fsub_rn(v[i + 1], mu);
-    q0 = __fmaf_rn(v[i], v[i], q0);
-    q1 = __fmaf_rn(v[i + 1], v[i + 1], q1);
+  for (int i = 0; i < 16; ++i) {
+    const float d0 = __fsub_rn(bf16lo(xw[i]), mu), d1 = __fsub_rn(bf16hi(xw[i]), mu);
+    q0 = __fmaf_rn(d0, d0, q0);
+    q1 = __fmaf_rn(d1, d1, q1);
   }
   float ss = q0 + q1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
   const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1024.f), eps)));
+  const uint4* g4 = reinterpret_cast<const uint4*>(g);
+  const uint4* b4 = reinterpret_cast<const uint4*>(b);
   uint4* yr = reinterpret_cast<uint4*>(y + row * 1024);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint32_t gw[4] = {gu[q].x, gu[q].y, gu[q].z, gu[q].w};
-    const uint32_t bw[4] = {bu[q].x, bu[q].y, bu[q].z, bu[q].w};
+    const uint4 gu = __ldg(g4 + q * 32 + lane), bu = __ldg(b4 + q * 32 + lane);
+    const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
+    const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float y0 = __fadd_rn(__fmul_rn(__fmul_rn(v[q * 8 + 2 * e], inv), bf16lo(gw[e])), bf16lo(bw[e]));
+      const uint32_t w = xw[4 * q + e];
+      const float y0 =
+          __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16lo(w), mu), inv), bf16lo(gw[e])), bf16lo(bw[e]));
       const float y1 =
-          __fadd_rn(__fmul_rn(__fmul_rn(v[q * 8 + 2 * e + 1], inv), bf16hi(gw[e])), bf16hi(bw[e]));
+          __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16hi(w), mu), inv), bf16hi(gw[e])), bf16hi(bw[e]));
       o[e] = pack_bf16x2(y0, y1);
     }
     yr[q * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);

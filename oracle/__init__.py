@@ -1,7 +1,9 @@
 """CPU oracle of the vision-tower encode.  TEST INFRASTRUCTURE ONLY.
 
 Only the test suite, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
-leg may import it; the product path never does.  See ``oracle/encode.py``.
+leg may import it; the product path never does.  See ``oracle/encode.py``;
+the image preprocessing upstream of the encode (grid plan, contain resize with
+bicubic filtering, gray canvas) is ``oracle/preprocess.py``.
 """
 from .encode import (TOK_END, TOK_IMAGE, TOK_NEWLINE, TOK_START, attention, bits_to_f32,
                      block_tail, encode, f32_to_bits, gelu, grid_positions, layer_norm,

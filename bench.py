@@ -267,6 +267,43 @@ def other_workloads(dw, cfg, pk, reps: int = 5):
     return res
 
 
+def preprocess_workloads(pk, reps: int = 20):
+    """The preprocessing step (plan, contain resize, gray canvas) on images off
+    the patch grid: CUDA-event time per image (median of `reps`, after warm-up)
+    and the algorithmic bytes (input read once, intermediate written and read
+    once when the width changes, canvas written once) against the measured HBM
+    copy bandwidth."""
+    import torch
+
+    import workloads as WL
+    import vit_vision_encoder_gb300 as dv
+    res = {}
+    for name, (H, W, kind, seed) in WL.PREPROCESS_WORKLOADS.items():
+        img = torch.from_numpy(WL.make_image(H, W, kind, seed)).cuda()
+        canvas, plan = dv.preprocess(img)
+        for _ in range(3):
+            dv.preprocess(img, canvas=canvas)
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dv.preprocess(img, canvas=canvas)
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / 1e3)
+        sec = statistics.median(per)
+        nbytes = H * W * 3 + plan["Hc"] * plan["Wc"] * 3
+        if plan["Wr"] != W:
+            nbytes += 2 * H * plan["Wr"] * 3
+        res[name] = {"input": [H, W], "grid": [plan["h"], plan["w"]], "canvas": [plan["Hc"], plan["Wc"]],
+                     "resized": [plan["Hr"], plan["Wr"]], "ms": round(sec * 1e3, 4),
+                     "algorithmic_bytes": nbytes, "gb_per_s": round(nbytes / sec / 1e9, 1),
+                     "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm"], 3),
+                     "note": "includes the per-call coefficient-table kernel (float64)"}
+    return res
+
+
 def run_profile_case(case: str):
     """A bounded case for ncu (run it with --profile-from-start off): warm-up
     launches, then exactly the launches of interest between
@@ -478,6 +515,7 @@ def main():
     }
     if not args.skip_workloads:
         line["workloads"] = other_workloads(dw, cfg, pk)
+        line["preprocess"] = preprocess_workloads(pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

@@ -115,7 +115,8 @@ const char* ds_vit_strerror(int code);
 /*
  * ds_vit_prepare: validate `cfg`, keep the weight pointers (they must stay
  * valid until ds_vit_release), allocate the device copies the kernels need
- * (patch weight padded from K=588 to K=640 with zero columns, [A] Step 5; the
+ * (patch weight reordered to the pixel order of each patch row and padded to
+ * 64 columns per patch row, K = 896, [A] Step 5; the
  * first merger weight with its input permuted from c*9+p to p*1024+c; the RoPE
  * cos/sin table; a device status word) and build the TMA descriptors.
  * Synchronises `stream` before returning.  On error *out is NULL.
@@ -125,6 +126,51 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w,
 
 /* Free what ds_vit_prepare allocated (device-synchronising).  NULL is a no-op. */
 int ds_vit_release(ds_vit_prepared* p);
+
+/*
+ * Image preprocessing upstream of the encode ([A] "Step 1: Reproduce the
+ * discrete image-processing rules"; [B] V4.1 paragraph: minimum pixel budget
+ * 295,936, at most 1,024 image tokens, no aspect clamp; Lucebox "Image input":
+ * bicubic resizing that matches Pillow byte for byte).
+ *
+ * ds_vit_plan_image (host only): the plan of an H x W image.  Unit u = 42
+ * pixels (patch 14 x merge 3).  An image under 295,936 pixels is first
+ * enlarged by s = sqrt(295936 / (H W)); the merged grid is (h, w) =
+ * (ceil(sH/u), ceil(sW/u)) when h*w <= 1024, otherwise the aspect-preserving
+ * floor grid under 1,024 tokens (each side >= 1).  Canvas Hc x Wc = hu x wu
+ * (patch grid 3h x 3w).  The image is resized to Hr x Wr with PIL "contain"
+ * rules (the side that does not fill the canvas is round(...), half to even)
+ * and placed at (y0, x0) = ((Hc - Hr)/2, (Wc - Wr)/2) rounded down; the rest of
+ * the canvas is RGB 127.  H, W in [1, 65535] with H*W <= 2^28, else
+ * DS_VIT_EINVAL.
+ */
+typedef struct ds_vit_plan {
+  int32_t H, W;     /* input image */
+  int32_t h, w;     /* merged grid: h*w image tokens (<= DS_VIT_MAX_TOKENS) */
+  int32_t Hc, Wc;   /* canvas pixels = 42h x 42w: the encode's H and W */
+  int32_t Hr, Wr;   /* resized image inside the canvas */
+  int32_t y0, x0;   /* top-left corner of the resized image */
+} ds_vit_plan;
+
+int ds_vit_plan_image(int32_t H, int32_t W, ds_vit_plan* out);
+
+/* Device workspace of ds_vit_preprocess for `plan` (host only). */
+int ds_vit_preprocess_workspace_bytes(const ds_vit_plan* plan, size_t* bytes);
+
+/*
+ * ds_vit_preprocess: pixels (device uint8 [H, W, 3], HWC RGB) -> canvas
+ * (device uint8 [Hc, Wc, 3]), ready for ds_vit_encode(canvas, Hc, Wc).
+ * Bicubic (Keys, a = -0.5, support 2 widened by the reduction factor), weights
+ * in float64 normalised per output pixel and rounded to 22 fraction bits;
+ * horizontal pass then vertical pass, each rounded and clamped to uint8
+ * ((2^21 + sum) >> 22); a pass whose size does not change is skipped.  The
+ * canvas is written completely.  `plan` must equal ds_vit_plan_image(H, W)
+ * (DS_VIT_EINVAL otherwise); ws: device workspace of at least
+ * ds_vit_preprocess_workspace_bytes (DS_VIT_ECAP otherwise).  Pixel, canvas
+ * and workspace memory stay caller-owned; nothing is written on an error.
+ */
+int ds_vit_preprocess(const ds_vit_plan* plan, const uint8_t* pixels, void* canvas, void* ws,
+                      size_t ws_bytes, void* stream);
 
 /*
  * ds_vit_layout (host only, no GPU needed): the token span of one image with a

@@ -80,6 +80,42 @@ def test_null_arguments_rejected_before_cuda(dv):
     assert L.ds_vit_op_linear(None, 1, 64, None, 256, None, None, 0, None, None, None, None) == dv.EINVAL
 
 
+def test_plan_matches_oracle(dv):
+    """The host planner of the C ABI agrees with the oracle's plan exactly
+    (every field), on the workload sizes and on random sizes up to 16000."""
+    import oracle.preprocess as PP
+    sizes = [(546, 546), (1344, 1344), (2688, 336), (544, 544), (100, 100), (3024, 4032),
+             (1080, 1920), (1000, 333), (20000, 100), (1, 1), (1, 65535), (65535, 1), (300, 100),
+             (100, 300), (4, 1), (4, 3)]
+    rng = np.random.default_rng(11)
+    sizes += [(int(h), int(w)) for h, w in rng.integers(1, 16000, (400, 2))]   # H*W <= 2^28
+    sizes += [(int(h), int(w)) for h, w in rng.integers(1, 700, (400, 2))]
+    for H, W in sizes:
+        got = dv.plan_image(H, W)
+        ref = PP.plan(H, W)
+        for k in ("h", "w", "Hc", "Wc", "Hr", "Wr", "y0", "x0"):
+            assert got[k] == ref[k], (H, W, k, got, ref)
+
+
+def test_plan_and_preprocess_argument_checks(dv):
+    L = dv.lib
+    p = dv.Plan()
+    for H, W in ((0, 10), (10, 0), (65536, 10), (20000, 20000)):
+        assert L.ds_vit_plan_image(H, W, C.byref(p)) == dv.EINVAL
+    assert L.ds_vit_plan_image(10, 10, None) == dv.EINVAL
+    assert L.ds_vit_plan_image(1000, 333, C.byref(p)) == dv.OK
+    b = C.c_size_t(0)
+    assert L.ds_vit_preprocess_workspace_bytes(C.byref(p), C.byref(b)) == dv.OK and b.value > 0
+    p.Hr += 1                                     # a plan that is not the image's plan
+    assert L.ds_vit_preprocess_workspace_bytes(C.byref(p), C.byref(b)) == dv.EINVAL
+    assert L.ds_vit_preprocess(C.byref(p), C.c_void_p(16), C.c_void_p(16), C.c_void_p(256), 1 << 30,
+                               None) == dv.EINVAL
+    p.Hr -= 1
+    assert L.ds_vit_preprocess(None, None, None, None, 0, None) == dv.EINVAL
+    assert L.ds_vit_preprocess(C.byref(p), C.c_void_p(16), C.c_void_p(16), C.c_void_p(256), 0,
+                               None) == dv.ECAP
+
+
 def test_workspace_size_validation(dv):
     # a non-multiple of 14 and an image over the 9216-patch limit are refused
     L = dv.lib

@@ -56,6 +56,10 @@ class Span(C.Structure):
                 ("embed_row", C.c_int64)]
 
 
+class Plan(C.Structure):
+    _fields_ = [(f, C.c_int32) for f in ("H", "W", "h", "w", "Hc", "Wc", "Hr", "Wr", "y0", "x0")]
+
+
 # Every symbol include/dsvit.h declares: name -> (restype, argtypes).
 _VP, _I32, _I64, _SZ, _F = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t, C.c_float
 _P_I32, _P_I64 = C.POINTER(C.c_int32), C.POINTER(C.c_int64)
@@ -81,6 +85,9 @@ SIGNATURES = {
     "ds_vit_op_linear": (C.c_int, [_VP, _I64, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
     "ds_vit_op_rope_table": (C.c_int, [_VP, _I32, _F, _VP]),
     "ds_vit_op_attention": (C.c_int, [_VP, _P_I32, C.c_int, _VP, _VP, _VP]),
+    "ds_vit_plan_image": (C.c_int, [_I32, _I32, C.POINTER(Plan)]),
+    "ds_vit_preprocess_workspace_bytes": (C.c_int, [C.POINTER(Plan), C.POINTER(_SZ)]),
+    "ds_vit_preprocess": (C.c_int, [C.POINTER(Plan), _VP, _VP, _VP, _SZ, _VP]),
 }
 
 
@@ -280,6 +287,32 @@ class Encoder:
 
     def status(self) -> int:
         return lib.ds_vit_device_status(self.handle, _stream())
+
+
+def plan_image(H: int, W: int) -> dict:
+    """Preprocessing plan of an H x W image (host call): grid, canvas, resized
+    size and placement (include/dsvit.h, ds_vit_plan_image)."""
+    p = Plan()
+    check(lib.ds_vit_plan_image(int(H), int(W), C.byref(p)), "ds_vit_plan_image")
+    return {f: int(getattr(p, f)) for f, _ in Plan._fields_}
+
+
+def preprocess(img, canvas=None):
+    """uint8 CUDA tensor [H, W, 3] -> (canvas uint8 CUDA tensor [Hc, Wc, 3], plan
+    dict): contain-resize with bicubic filtering onto the RGB 127 canvas."""
+    torch = _torch()
+    H, W = int(img.shape[0]), int(img.shape[1])
+    p = Plan()
+    check(lib.ds_vit_plan_image(H, W, C.byref(p)), "ds_vit_plan_image")
+    nbytes = C.c_size_t()
+    check(lib.ds_vit_preprocess_workspace_bytes(C.byref(p), C.byref(nbytes)),
+          "ds_vit_preprocess_workspace_bytes")
+    ws = torch.empty(max(int(nbytes.value), 256), dtype=torch.uint8, device="cuda")
+    if canvas is None:
+        canvas = torch.empty((p.Hc, p.Wc, 3), dtype=torch.uint8, device="cuda")
+    check(lib.ds_vit_preprocess(C.byref(p), _ptr(img), _ptr(canvas), _ptr(ws), ws.numel(), _stream()),
+          "ds_vit_preprocess")
+    return canvas, {f: int(getattr(p, f)) for f, _ in Plan._fields_}
 
 
 def overlay(hidden, spans, embeds, sentinel):

@@ -108,6 +108,16 @@ def gradient_image(H: int, W: int, seed: int) -> np.ndarray:
     return np.clip(np.rint(img), 0, 255).astype(np.uint8)
 
 
+# Inputs of the preprocessing step (plan, contain resize, gray canvas): images
+# off the patch grid, as a camera or a rendered chart delivers them.
+#   photo: 3024 x 4032 (H x W) gradient + noise, seed 6 -> 27 x 36 merged grid;
+#   chart: 600 x 800 uniform, seed 7 -> 15 x 20 grid (resized up by 1.05).
+PREPROCESS_WORKLOADS = {
+    "photo": (3024, 4032, "gradient", 6),
+    "chart": (600, 800, "uniform", 7),
+}
+
+
 def hidden_buffer(rows: int, width: int, seed: int) -> np.ndarray:
     """Prompt hidden states ~ N(0, 1) as bf16 bit patterns."""
     return to_bf16_bits(_rng(seed).standard_normal((rows, width), dtype=np.float32))

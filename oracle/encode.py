@@ -371,6 +371,33 @@ def layout(gh: int, gw: int, image_token_id: int, base_pos: int = 0, m: int = 3)
     return ids, pos, np.asarray(types, dtype=np.uint8), np.asarray(src, dtype=np.int32)
 
 
+def overlay_chunk(chunk: np.ndarray, chunk_begin: int, spans, embeds, sentinel):
+    """Overlay for chunked prefill (page A, "Connect the complete image-to-text
+    path first": an image span may cross a chunk boundary, so the engine keeps
+    each image's token range and, when it assembles an embedding chunk, replaces
+    only the intersecting part; page A's routing section: a row-level
+    image-rows mask travels with the rows).
+
+    chunk: [R, width] bit patterns of prompt rows chunk_begin .. chunk_begin+R-1;
+    spans: (base_row, gh, gw, embed_row) per image, spans in prompt rows.
+    Returns the chunk with every span row inside it written as ``overlay``
+    writes it, and row_type uint8 [R]: 0 for rows outside every span, 1 + the
+    layout type (START 1, IMAGE 2, NEWLINE 3, END 4) for span rows."""
+    out = np.array(chunk, copy=True)
+    row_type = np.zeros(out.shape[0], dtype=np.uint8)
+    for base, gh, gw, erow in spans:
+        _, _, types, src = layout(gh, gw, 0)
+        for r, (t, s) in enumerate(zip(types, src)):
+            i = base + r - chunk_begin
+            if 0 <= i < out.shape[0]:
+                if t == TOK_IMAGE:
+                    out[i] = embeds[erow + s]
+                else:
+                    out[i] = sentinel[{TOK_START: 0, TOK_NEWLINE: 1, TOK_END: 2}[int(t)]]
+                row_type[i] = 1 + int(t)
+    return out, row_type
+
+
 def overlay(hidden: np.ndarray, base_row: int, types, src, embeds, sentinel) -> np.ndarray:
     """Copy of ``hidden`` (bf16 bit patterns) with the span written at base_row:
     IMAGE rows take aligner rows ``embeds[src]``; START / NEWLINE / END rows take

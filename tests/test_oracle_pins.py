@@ -485,3 +485,47 @@ def test_overlay_exact_and_untouched():
     assert np.array_equal(out[10], sent[0]) and np.array_equal(out[10 + n - 1], sent[2])
     assert np.array_equal(out[11:14], emb[0:3]) and np.array_equal(out[14], sent[1])
     assert np.array_equal(out[15:18], emb[3:6]) and np.array_equal(out[18], sent[1])
+
+
+def _two_span_prompt(rng, rows=120, width=16):
+    """Prompt with two spans (2x3 and 3x2 merged grids) and text around them."""
+    hidden = rng.integers(0, 65535, size=(rows, width), dtype=np.uint16)
+    emb = rng.integers(0, 65535, size=(12, width), dtype=np.uint16)
+    sent = rng.integers(0, 65535, size=(3, width), dtype=np.uint16)
+    spans = [(7, 6, 9, 0), (50, 9, 6, 6)]          # (base_row, gh, gw, embed_row)
+    return hidden, emb, sent, spans
+
+
+def test_overlay_chunks_assemble_to_the_whole_prompt():
+    """Page A: a span may cross a chunk boundary and each chunk replaces only
+    the intersecting rows.  Any split of the prompt into chunks, overlaid
+    chunk by chunk, equals the whole-prompt overlay (pinned above), and the
+    row types are the layout's types on span rows, 0 elsewhere."""
+    rng = np.random.default_rng(29)
+    hidden, emb, sent, spans = _two_span_prompt(rng)
+    whole = hidden
+    want_type = np.zeros(len(hidden), dtype=np.uint8)
+    for base, gh, gw, erow in spans:
+        _, _, typ, src = O.layout(gh, gw, 1)
+        src = np.where(src >= 0, src + erow, src)
+        whole = O.overlay(whole, base, typ, src, emb, sent)
+        want_type[base:base + len(typ)] = typ + 1
+    for cuts in ([0, 120], [0, 9, 120], [0, 8, 13, 51, 52, 60, 119, 120], list(range(0, 121, 5)),
+                 [0, 1, 2, 3, 120]):
+        parts, types = [], []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            out, rt = O.overlay_chunk(hidden[a:b], a, spans, emb, sent)
+            parts.append(out)
+            types.append(rt)
+        assert np.array_equal(np.concatenate(parts), whole)
+        assert np.array_equal(np.concatenate(types), want_type)
+
+
+def test_overlay_chunk_outside_spans_is_untouched():
+    rng = np.random.default_rng(31)
+    hidden, emb, sent, spans = _two_span_prompt(rng)
+    out, rt = O.overlay_chunk(hidden[20:50], 20, spans, emb, sent)    # between the spans
+    assert np.array_equal(out, hidden[20:50]) and not rt.any()
+    out, rt = O.overlay_chunk(hidden[5:8], 5, spans, emb, sent)       # one START row at 7
+    assert np.array_equal(out[:2], hidden[5:7]) and np.array_equal(out[2], sent[0])
+    assert list(rt) == [0, 0, 1 + O.TOK_START]

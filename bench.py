@@ -304,6 +304,51 @@ def preprocess_workloads(pk, reps: int = 20):
     return res
 
 
+def overlay_chunk_timing(pk, chunk_rows: int = 2048, reps: int = 20):
+    """Chunked-prefill overlay of the 16-image batch prompt (16384 x 5120, 16
+    spans, 6436 span rows) in chunks of `chunk_rows`, with the row-type mask:
+    CUDA-event time for all chunks (median of `reps`) and algorithmic bytes
+    (each span row read once and written once, one mask byte per prompt row)."""
+    import numpy as np
+    import torch
+
+    import oracle as O
+    import workloads as WL
+    import vit_vision_encoder_gb300 as dv
+    sizes = [(H, W) for H, W, _, _ in WL.WORKLOADS["batch16"]["images"]]
+    rows = [len(O.layout(H // 14, W // 14, 1)[0]) for H, W in sizes]
+    ntok = [((H // 14 + 2) // 3) * ((W // 14 + 2) // 3) for H, W in sizes]
+    bases = WL.span_bases("batch16", rows)
+    eoff = np.concatenate([[0], np.cumsum(ntok)])
+    spans = [(bases[i], H // 14, W // 14, int(eoff[i])) for i, (H, W) in enumerate(sizes)]
+    hidden = torch.randn((16384, 5120), device="cuda").to(torch.bfloat16)
+    emb = torch.randn((int(eoff[-1]), 5120), device="cuda").to(torch.bfloat16)
+    sent = torch.randn((3, 5120), device="cuda").to(torch.bfloat16)
+    mask = torch.empty(16384, dtype=torch.uint8, device="cuda")
+    chunks = [(a, min(a + chunk_rows, 16384)) for a in range(0, 16384, chunk_rows)]
+
+    def run():
+        for a, b in chunks:
+            dv.overlay_chunk(hidden[a:b], a, spans, emb, sent, row_type=mask[a:b])
+
+    for _ in range(3):
+        run()
+    torch.cuda.synchronize()
+    per = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        per.append(e0.elapsed_time(e1) / 1e3)
+    sec = statistics.median(per)
+    nbytes = sum(rows) * 5120 * 2 * 2 + 16384
+    return {"prompt_rows": 16384, "span_rows": sum(rows), "chunk_rows": chunk_rows, "chunks": len(chunks),
+            "ms": round(sec * 1e3, 4), "algorithmic_bytes": nbytes, "gb_per_s": round(nbytes / sec / 1e9, 1),
+            "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm"], 3)}
+
+
 def run_profile_case(case: str):
     """A bounded case for ncu (run it with --profile-from-start off): warm-up
     launches, then exactly the launches of interest between
@@ -516,6 +561,7 @@ def main():
     if not args.skip_workloads:
         line["workloads"] = other_workloads(dw, cfg, pk)
         line["preprocess"] = preprocess_workloads(pk)
+        line["overlay_chunks"] = overlay_chunk_timing(pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

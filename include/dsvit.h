@@ -278,6 +278,27 @@ int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_s
                    int n_spans, const void* embeds, int64_t n_embeds, const void* sentinel,
                    void* stream);
 
+/*
+ * ds_vit_overlay_chunk: the overlay for chunked prefill ([A] "Connect the
+ * complete image-to-text path first": an image span may cross a chunk
+ * boundary, so each embedding chunk replaces only the rows of the spans that
+ * intersect it; [A]'s routing section: a row-level image-rows mask).
+ *   chunk:       device bf16 [chunk_rows, width], prompt rows
+ *                chunk_begin .. chunk_begin + chunk_rows - 1 (chunk_rows >= 1).
+ *   spans:       as ds_vit_overlay, in prompt rows (base_row >= 0); they may
+ *                extend past the chunk; embed rows inside [0, n_embeds); no overlap.
+ *   row_type:    device uint8 [chunk_rows] or NULL: 0 for rows outside every
+ *                span, 1 + the layout type for span rows (START 1, IMAGE 2,
+ *                NEWLINE 3, END 4); the image-rows mask is row_type != 0.
+ * Span rows inside the chunk are written exactly as ds_vit_overlay writes
+ * them; the other rows of the chunk are not touched.  Overlaying every chunk
+ * of a prompt equals one ds_vit_overlay of the whole prompt.
+ */
+int ds_vit_overlay_chunk(void* chunk, int64_t chunk_begin, int64_t chunk_rows, int32_t width,
+                         const ds_vit_span* spans, int n_spans, const void* embeds,
+                         int64_t n_embeds, const void* sentinel, uint8_t* row_type,
+                         void* stream);
+
 /* Kernel kinds reported by ds_vit_set_kernel_timer. */
 /* PATCH_GEMM patchifies and normalises the pixels inside its A-tile load;
  * MERGER_GEMM1 gathers the 3x3 windows inside its A-tile load. */

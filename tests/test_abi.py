@@ -73,6 +73,15 @@ def test_null_arguments_rejected_before_cuda(dv):
     w = dv.Weights()
     assert L.ds_vit_prepare(C.byref(bad), C.byref(w), C.byref(h), None) == dv.EINVAL
     assert L.ds_vit_overlay(None, 10, 5120, None, 1, None, 1, None, None) == dv.EINVAL
+    sp = (dv.Span * 2)()
+    sp[0].base_row, sp[0].gh, sp[0].gw, sp[0].embed_row = 10, 6, 6, 0
+    sp[1].base_row, sp[1].gh, sp[1].gw, sp[1].embed_row = 12, 6, 6, 4        # overlaps span 0
+    ok = C.c_void_p(256)
+    assert L.ds_vit_overlay_chunk(None, 0, 4, 5120, sp, 1, ok, 4, ok, None, None) == dv.EINVAL
+    assert L.ds_vit_overlay_chunk(ok, -1, 4, 5120, sp, 1, ok, 4, ok, None, None) == dv.EINVAL
+    assert L.ds_vit_overlay_chunk(ok, 0, 0, 5120, sp, 1, ok, 4, ok, None, None) == dv.EINVAL
+    assert L.ds_vit_overlay_chunk(ok, 0, 4, 5120, sp, 2, ok, 8, ok, None, None) == dv.EINVAL
+    assert L.ds_vit_overlay_chunk(ok, 0, 4, 5120, sp, 1, ok, 3, ok, None, None) == dv.ERANGE
     assert L.ds_vit_encode(None, None, 84, 84, None, None, 0, None) == dv.EINVAL
     assert L.ds_vit_release(None) == dv.OK
     assert L.ds_vit_device_status(None, None) == dv.EINVAL

@@ -197,6 +197,35 @@ def test_overlay_batch16_exact(dv, w32):
     assert np.array_equal(h.view(torch.int16).cpu().numpy().view(np.uint16), ref)
 
 
+def test_overlay_chunks_batch16_exact(dv, w32):
+    """Chunked prefill over the 16-span prompt: chunks of 2048 rows and a
+    ragged split (spans cross chunk boundaries) against the oracle, chunk by
+    chunk, with the row-type mask; the chunks reassemble to the whole overlay."""
+    sizes = [(H, W) for H, W, _, _ in WL.WORKLOADS["batch16"]["images"]]
+    lays = [O.layout(H // 14, W // 14, 1) for H, W in sizes]
+    bases = WL.span_bases("batch16", [len(l[0]) for l in lays])
+    ntok = [int((l[2] == O.TOK_IMAGE).sum()) for l in lays]
+    eoff = np.concatenate([[0], np.cumsum(ntok)])
+    hidden = WL.hidden_buffer(16384, 5120, WL.WORKLOADS["batch16"]["hidden_seed"])
+    emb = WL.hidden_buffer(int(eoff[-1]), 5120, 78)
+    spans = [(bases[i], H // 14, W // 14, int(eoff[i])) for i, (H, W) in enumerate(sizes)]
+    d_emb, d_sent = dev(emb, torch), dev(w32["sentinel"], torch)
+    whole = dev(hidden, torch)
+    dv.overlay(whole, spans, d_emb, d_sent)
+    for cuts in (list(range(0, 16385, 2048)), [0, 65, 700, 701, 3000, 6979, 6980, 16384]):
+        parts = []
+        for a, b in zip(cuts[:-1], cuts[1:]):
+            ch = dev(hidden[a:b], torch)
+            rt = torch.full((b - a,), 255, dtype=torch.uint8, device="cuda")
+            dv.overlay_chunk(ch, a, spans, d_emb, d_sent, row_type=rt)
+            torch.cuda.synchronize()
+            ref, ref_rt = O.overlay_chunk(hidden[a:b], a, spans, emb, w32["sentinel"])
+            assert np.array_equal(ch.view(torch.int16).cpu().numpy().view(np.uint16), ref), (a, b)
+            assert np.array_equal(rt.cpu().numpy(), ref_rt), (a, b)
+            parts.append(ch)
+        assert torch.equal(torch.cat(parts).view(torch.int16), whole.view(torch.int16))
+
+
 def test_overlay_rejects_out_of_range(dv, w32):
     h = torch.zeros((100, 5120), dtype=torch.bfloat16, device="cuda")
     emb = torch.zeros((4, 5120), dtype=torch.bfloat16, device="cuda")

@@ -79,6 +79,8 @@ SIGNATURES = {
     "ds_vit_encode_debug": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,
                                       _VP, _SZ, _VP, _VP, _VP]),
     "ds_vit_overlay": (C.c_int, [_VP, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP, _VP]),
+    "ds_vit_overlay_chunk": (C.c_int, [_VP, _I64, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP,
+                                       _VP, _VP]),
     "ds_vit_device_status": (C.c_int, [_VP, _VP]),
     "ds_vit_set_kernel_timer": (C.c_int, [_VP, C.POINTER(_VP), _P_I32, _I32, _P_I32]),
     "ds_vit_op_layernorm": (C.c_int, [_VP, _VP, _VP, _VP, _I64, _F, _VP]),
@@ -323,6 +325,20 @@ def overlay(hidden, spans, embeds, sentinel):
     check(lib.ds_vit_overlay(_ptr(hidden), hidden.shape[0], hidden.shape[1], arr, len(spans),
                              _ptr(embeds), embeds.shape[0], _ptr(sentinel), _stream()),
           "ds_vit_overlay")
+
+
+def overlay_chunk(chunk, chunk_begin, spans, embeds, sentinel, row_type=None):
+    """Chunked prefill: ``chunk`` holds prompt rows chunk_begin.. (in place);
+    spans as ``overlay``.  row_type (uint8 CUDA tensor [rows], optional)
+    receives 0 for text rows and 1 + the layout type for span rows."""
+    arr = (Span * len(spans))()
+    for i, (b, gh, gw, e) in enumerate(spans):
+        arr[i].base_row, arr[i].gh, arr[i].gw, arr[i].embed_row = b, gh, gw, e
+    check(lib.ds_vit_overlay_chunk(_ptr(chunk), int(chunk_begin), chunk.shape[0], chunk.shape[1], arr,
+                                   len(spans), _ptr(embeds), embeds.shape[0], _ptr(sentinel),
+                                   _ptr(row_type), _stream()),
+          "ds_vit_overlay_chunk")
+    return row_type
 
 
 # ---------------------------------------------------------------- single kernels

@@ -274,6 +274,33 @@ int encode_common(const ds_vit_prepared* p, int n, const uint8_t* const* pixels,
                     static_cast<bf16*>(final_norm), static_cast<cudaStream_t>(stream));
 }
 
+// Validated device-side description of the spans of one overlay call.  Spans
+// must have positive grids, embed rows inside [0, n_embeds), base_row >= 0,
+// rows inside [0, n_hidden) when n_hidden >= 0, and must not overlap.
+int build_spans(const ds_vit_span* spans, int n_spans, int64_t n_embeds, int64_t n_hidden,
+                OverlaySpans* os) {
+  if (!spans || n_spans < 1 || n_spans > DS_VIT_MAX_IMAGES || n_embeds < 0) return DS_VIT_EINVAL;
+  os->n = n_spans;
+  std::vector<std::pair<int64_t, int64_t>> ranges;
+  for (int s = 0; s < n_spans; ++s) {
+    const ds_vit_span& sp = spans[s];
+    if (sp.gh <= 0 || sp.gw <= 0) return DS_VIT_EINVAL;
+    const int64_t h = (sp.gh + 2) / 3, w = (sp.gw + 2) / 3, rows = 2 + h * (w + 1);
+    if (sp.base_row < 0 || (n_hidden >= 0 && sp.base_row + rows > n_hidden)) return DS_VIT_ERANGE;
+    if (sp.embed_row < 0 || sp.embed_row + h * w > n_embeds) return DS_VIT_ERANGE;
+    os->base_row[s] = sp.base_row;
+    os->embed_row[s] = sp.embed_row;
+    os->h[s] = static_cast<int>(h);
+    os->w[s] = static_cast<int>(w);
+    os->row_start[s + 1] = os->row_start[s] + rows;
+    ranges.emplace_back(sp.base_row, sp.base_row + rows);
+  }
+  std::sort(ranges.begin(), ranges.end());
+  for (size_t i = 1; i < ranges.size(); ++i)
+    if (ranges[i].first < ranges[i - 1].second) return DS_VIT_EINVAL;
+  return DS_VIT_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -455,31 +482,28 @@ int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* con
 int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_span* spans,
                    int n_spans, const void* embeds, int64_t n_embeds, const void* sentinel,
                    void* stream) {
-  if (!hidden || !spans || !embeds || !sentinel || n_spans < 1 || n_spans > DS_VIT_MAX_IMAGES ||
-      width <= 0 || width % 8 != 0 || n_hidden <= 0 || n_embeds < 0)
+  if (!hidden || !embeds || !sentinel || width <= 0 || width % 8 != 0 || n_hidden <= 0)
     return DS_VIT_EINVAL;
   if (!aligned16(hidden) || !aligned16(embeds) || !aligned16(sentinel)) return DS_VIT_EINVAL;
   OverlaySpans os{};
-  os.n = n_spans;
-  std::vector<std::pair<int64_t, int64_t>> ranges;
-  for (int s = 0; s < n_spans; ++s) {
-    const ds_vit_span& sp = spans[s];
-    if (sp.gh <= 0 || sp.gw <= 0) return DS_VIT_EINVAL;
-    const int64_t h = (sp.gh + 2) / 3, w = (sp.gw + 2) / 3, rows = 2 + h * (w + 1);
-    if (sp.base_row < 0 || sp.base_row + rows > n_hidden) return DS_VIT_ERANGE;
-    if (sp.embed_row < 0 || sp.embed_row + h * w > n_embeds) return DS_VIT_ERANGE;
-    os.base_row[s] = sp.base_row;
-    os.embed_row[s] = sp.embed_row;
-    os.h[s] = static_cast<int>(h);
-    os.w[s] = static_cast<int>(w);
-    os.row_start[s + 1] = os.row_start[s] + rows;
-    ranges.emplace_back(sp.base_row, sp.base_row + rows);
-  }
-  std::sort(ranges.begin(), ranges.end());
-  for (size_t i = 1; i < ranges.size(); ++i)
-    if (ranges[i].first < ranges[i - 1].second) return DS_VIT_EINVAL;
+  DSV_TRY(build_spans(spans, n_spans, n_embeds, n_hidden, &os));
   return launch_overlay(static_cast<bf16*>(hidden), width, os, static_cast<const bf16*>(embeds),
                         static_cast<const bf16*>(sentinel), static_cast<cudaStream_t>(stream));
+}
+
+int ds_vit_overlay_chunk(void* chunk, int64_t chunk_begin, int64_t chunk_rows, int32_t width,
+                         const ds_vit_span* spans, int n_spans, const void* embeds,
+                         int64_t n_embeds, const void* sentinel, uint8_t* row_type,
+                         void* stream) {
+  if (!chunk || !embeds || !sentinel || width <= 0 || width % 8 != 0 || chunk_begin < 0 ||
+      chunk_rows < 1 || chunk_rows > INT32_MAX)
+    return DS_VIT_EINVAL;
+  if (!aligned16(chunk) || !aligned16(embeds) || !aligned16(sentinel)) return DS_VIT_EINVAL;
+  OverlaySpans os{};
+  DSV_TRY(build_spans(spans, n_spans, n_embeds, -1, &os));
+  return launch_overlay_chunk(static_cast<bf16*>(chunk), chunk_begin, chunk_rows, width, os,
+                              static_cast<const bf16*>(embeds), static_cast<const bf16*>(sentinel),
+                              row_type, static_cast<cudaStream_t>(stream));
 }
 
 int ds_vit_set_kernel_timer(ds_vit_prepared* p, void* const* events, int32_t* kinds,

@@ -145,5 +145,8 @@ struct OverlaySpans {
 
 int launch_overlay(bf16* hidden, int width, const OverlaySpans& spans, const bf16* embeds,
                    const bf16* sentinel, cudaStream_t stream);
+int launch_overlay_chunk(bf16* chunk, int64_t chunk_begin, int64_t chunk_rows, int width,
+                         const OverlaySpans& spans, const bf16* embeds, const bf16* sentinel,
+                         uint8_t* row_type, cudaStream_t stream);
 
 }  // namespace dsvit

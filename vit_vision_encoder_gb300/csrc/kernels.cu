@@ -149,6 +149,56 @@ __global__ void __launch_bounds__(128) overlay_kernel(bf16* __restrict__ hidden,
   for (int k = threadIdx.x; k < width / 8; k += blockDim.x) d4[k] = s4[k];
 }
 
+// Chunked prefill: one block per chunk row g = chunk_begin + i.  The span that
+// holds g (if any) gives the row's source as in overlay_kernel and its type
+// code 1 + type; rows outside every span keep their contents, type 0.
+__global__ void __launch_bounds__(128) overlay_chunk_kernel(bf16* __restrict__ chunk, int64_t chunk_begin,
+                                                            int width,
+                                                            const __grid_constant__ OverlaySpans spans,
+                                                            const bf16* __restrict__ embeds,
+                                                            const bf16* __restrict__ sentinel,
+                                                            uint8_t* __restrict__ row_type) {
+  const int64_t i = blockIdx.x;
+  const int64_t g = chunk_begin + i;
+  int s = -1;
+  for (int k = 0; k < spans.n; ++k) {
+    const int64_t n = spans.row_start[k + 1] - spans.row_start[k];
+    if (g >= spans.base_row[k] && g < spans.base_row[k] + n) {
+      s = k;
+      break;
+    }
+  }
+  if (s < 0) {
+    if (row_type && threadIdx.x == 0) row_type[i] = 0;
+    return;
+  }
+  const int64_t r = g - spans.base_row[s];
+  const int64_t n = spans.row_start[s + 1] - spans.row_start[s];
+  const int w = spans.w[s];
+  const bf16* src;
+  int type;
+  if (r == 0) {
+    src = sentinel;
+    type = DS_VIT_TOK_START;
+  } else if (r == n - 1) {
+    src = sentinel + 2 * static_cast<int64_t>(width);
+    type = DS_VIT_TOK_END;
+  } else {
+    const int64_t q = r - 1, y = q / (w + 1), x = q % (w + 1);
+    if (x == w) {
+      src = sentinel + width;
+      type = DS_VIT_TOK_NEWLINE;
+    } else {
+      src = embeds + (spans.embed_row[s] + y * w + x) * width;
+      type = DS_VIT_TOK_IMAGE;
+    }
+  }
+  if (row_type && threadIdx.x == 0) row_type[i] = static_cast<uint8_t>(1 + type);
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  uint4* d4 = reinterpret_cast<uint4*>(chunk + i * width);
+  for (int k = threadIdx.x; k < width / 8; k += blockDim.x) d4[k] = s4[k];
+}
+
 }  // namespace
 
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
@@ -178,6 +228,14 @@ int launch_permute_m1(const bf16* w, bf16* w_perm, int rows, cudaStream_t stream
 
 int launch_pad_patch_w(const bf16* w, bf16* w_pad, int rows, cudaStream_t stream) {
   pad_patch_w_kernel<<<rows, 128, 0, stream>>>(w, w_pad);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_overlay_chunk(bf16* chunk, int64_t chunk_begin, int64_t chunk_rows, int width,
+                         const OverlaySpans& spans, const bf16* embeds, const bf16* sentinel,
+                         uint8_t* row_type, cudaStream_t stream) {
+  overlay_chunk_kernel<<<static_cast<unsigned>(chunk_rows), 128, 0, stream>>>(chunk, chunk_begin, width, spans,
+                                                                              embeds, sentinel, row_type);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 

@@ -7,7 +7,8 @@ bicubic filtering, gray canvas) is ``oracle/preprocess.py``.
 """
 from .encode import (TOK_END, TOK_IMAGE, TOK_NEWLINE, TOK_START, attention, bits_to_f32,
                      block_tail, encode, f32_to_bits, gelu, grid_positions, layer_norm,
-                     layout, merge_unfold, merger, mm, normalise, overlay, overlay_chunk, patchify, products,
+                     layout, merge_unfold, merger, mlp_hidden, mm, norm, normalise, overlay, overlay_chunk,
+                     patchify, products, rms_norm, rope_half_vector, silu,
                      qkv_project,
                      rope, rope_angles, rope_freqs, round_bf16, softmax_rows, unpatchify,
                      vit_block)

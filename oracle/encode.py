@@ -157,6 +157,21 @@ def rope_angles(gy: np.ndarray, gx: np.ndarray, theta: float) -> np.ndarray:
                            np.asarray(gx, np.float64)[:, None] * f[None, :]], axis=1)
 
 
+def rope_half_vector(v: np.ndarray, gy: np.ndarray, gx: np.ndarray, theta: float) -> np.ndarray:
+    """Page A's pairing, taken literally ("Step 3": the angle vector
+    [h*f0..h*fn, w*f0..w*fn] with the half-vector rotation convention): per
+    head, dim i (i < 32) pairs with dim i + 32 and the pair turns by angle
+    ang[i] of rope_angles:  v'[i] = v[i] cos - v[i+32] sin,
+    v'[i+32] = v[i+32] cos + v[i] sin.  fp32 rotation, float64 cos/sin."""
+    n = v.shape[0]
+    ang = rope_angles(gy, gx, theta)                      # [n, 32]
+    cos = np.cos(ang).astype(F32)[:, None, :]
+    sin = np.sin(ang).astype(F32)[:, None, :]
+    h = v.reshape(n, -1, 64)
+    a, b = h[:, :, :32], h[:, :, 32:]
+    return np.concatenate([a * cos - b * sin, b * cos + a * sin], axis=2).reshape(n, -1)
+
+
 def rope(v: np.ndarray, gy: np.ndarray, gx: np.ndarray, theta: float) -> np.ndarray:
     """Rotate one projection (q or k), fp32 [n, heads*64] -> fp32 [n, heads*64].
 
@@ -192,6 +207,29 @@ def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float) -> np.nd
     var = (d * d).mean(axis=-1, dtype=F32, keepdims=True)
     inv = F32(1.0) / np.sqrt(var + F32(eps))
     return d * inv * g.astype(F32) + b.astype(F32)
+
+
+def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """x * (1/sqrt(mean(x^2) + eps)) * g over the last axis, fp32 (page A's
+    comparison table: the official vision tower uses RMSNorm; "Step 2" table:
+    "RMSNorm semantics" at the final norm output)."""
+    x = x.astype(F32)
+    ms = (x * x).mean(axis=-1, dtype=F32, keepdims=True)
+    inv = F32(1.0) / np.sqrt(ms + F32(eps))
+    return x * inv * g.astype(F32)
+
+
+def norm(x: np.ndarray, g, b, cfg: dict) -> np.ndarray:
+    """The block / final norm of the model variant: LayerNorm (default) or RMSNorm."""
+    if cfg.get("norm", "layernorm") == "rmsnorm":
+        return rms_norm(x, _f(g), cfg["ln_eps"])
+    return layer_norm(x, _f(g), _f(b), cfg["ln_eps"])
+
+
+def silu(z: np.ndarray) -> np.ndarray:
+    """z * sigmoid(z) = z / (1 + exp(-z)), float64, returned as fp32."""
+    zz = np.asarray(z, dtype=np.float64)
+    return (zz / (1.0 + np.exp(-zz))).astype(F32)
 
 
 def gelu(z: np.ndarray) -> np.ndarray:
@@ -239,19 +277,31 @@ def qkv_project(y, L, cfg, gy, gx):
     residual order); page B's table: no QK norm."""
     D = cfg["hidden"]
     t = mm(y, _f(L["qkv_w"]).T) + _f(L["qkv_b"])
-    q = round_bf16(rope(t[:, :D], gy, gx, cfg["rope_theta"]))
-    k = round_bf16(rope(t[:, D:2 * D], gy, gx, cfg["rope_theta"]))
+    rot = rope_half_vector if cfg.get("rope_pairing", "axis_halves") == "half_vector" else rope
+    q = round_bf16(rot(t[:, :D], gy, gx, cfg["rope_theta"]))
+    k = round_bf16(rot(t[:, D:2 * D], gy, gx, cfg["rope_theta"]))
     v = round_bf16(t[:, 2 * D:])
     return q, k, v
 
 
+def mlp_hidden(y, L, cfg):
+    """The MLP's stored hidden activation.  GELU MLP (default): r(GELU(y W_1^T +
+    b_1)).  SwiGLU (page A's comparison table for the official tower): W_1 and
+    b_1 hold the gate rows first and the up rows second, each ``mlp`` rows;
+    r(SiLU(y W_gate^T + b_gate) * (y W_up^T + b_up)), the product in fp32."""
+    t = mm(y, _f(L["fc1_w"]).T) + _f(L["fc1_b"])
+    if cfg.get("mlp_kind", "gelu") == "swiglu":
+        F = cfg["mlp"]
+        return round_bf16(silu(t[:, :F]) * t[:, F:2 * F])
+    return round_bf16(gelu(t))
+
+
 def block_tail(x_rows, o_rows, L, cfg):
-    """x = r(x + (o W_o^T + b_o)); y = r(LN2(x)); g = r(GELU(y W_1^T + b_1));
+    """x = r(x + (o W_o^T + b_o)); y = r(norm2(x)); g = mlp_hidden(y);
     x = r(x + (g W_2^T + b_2)).  Every stored activation is bf16 (page B)."""
-    eps = cfg["ln_eps"]
     x = round_bf16(x_rows + (mm(o_rows, _f(L["proj_w"]).T) + _f(L["proj_b"])))
-    y = round_bf16(layer_norm(x, _f(L["ln2_g"]), _f(L["ln2_b"]), eps))
-    g = round_bf16(gelu(mm(y, _f(L["fc1_w"]).T) + _f(L["fc1_b"])))
+    y = round_bf16(norm(x, L["ln2_g"], L["ln2_b"], cfg))
+    g = mlp_hidden(y, L, cfg)
     return round_bf16(x + (mm(g, _f(L["fc2_w"]).T) + _f(L["fc2_b"])))
 
 
@@ -264,7 +314,7 @@ def vit_block(x, L, cfg, seqlens, gy, gx, rows=None):
     values still come from every patch of the row's image).
     """
     heads = cfg["heads"]
-    y = round_bf16(layer_norm(x, _f(L["ln1_g"]), _f(L["ln1_b"]), cfg["ln_eps"]))
+    y = round_bf16(norm(x, L["ln1_g"], L["ln1_b"], cfg))
     q, k, v = qkv_project(y, L, cfg, gy, gx)
     starts = np.concatenate([[0], np.cumsum(seqlens)]).astype(np.int64)
     sel = np.arange(x.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
@@ -335,7 +385,7 @@ def encode(images, W: dict, cfg: dict, n_layers: int | None = None, dump: dict |
         x = vit_block(x, L, cfg, seqlens, gy, gx)
         if dump is not None:
             dump["blocks"].append(x)
-    z = round_bf16(layer_norm(x, _f(W["lnm_g"]), _f(W["lnm_b"]), cfg["ln_eps"]))
+    z = round_bf16(norm(x, W["lnm_g"], W["lnm_b"], cfg))
     starts = np.concatenate([[0], np.cumsum(seqlens)])
     A = np.concatenate([merge_unfold(z[starts[i]:starts[i + 1]], *grids[i], cfg["merge"])
                         for i in range(len(images))])

@@ -89,8 +89,7 @@ def assert_steps_teacher_forced(imgs, W, cfg, blocks, fnorm, out, layers, rows=N
         ref = O.vit_block(xin, W["layers"][l], cfg, seqlens, gy, gx, rows=rows)
         assert_parity(xout[sel], ref, what=f"block {l}")
     L = len(bl) - 1
-    z = O.round_bf16(O.layer_norm(bits_of(bl[L])[sel], O.bits_to_f32(W["lnm_g"]),
-                                  O.bits_to_f32(W["lnm_b"]), cfg["ln_eps"]))
+    z = O.round_bf16(O.norm(bits_of(bl[L])[sel], W["lnm_g"], W["lnm_b"], cfg))
     zg = fnorm.float().cpu().numpy()
     assert_parity(zg[sel], z, what="final norm")
     starts = np.concatenate([[0], np.cumsum(seqlens)])

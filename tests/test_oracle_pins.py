@@ -529,3 +529,88 @@ def test_overlay_chunk_outside_spans_is_untouched():
     out, rt = O.overlay_chunk(hidden[5:8], 5, spans, emb, sent)       # one START row at 7
     assert np.array_equal(out[:2], hidden[5:7]) and np.array_equal(out[2], sent[0])
     assert list(rt) == [0, 0, 1 + O.TOK_START]
+
+
+# ------------------------------------------------------------------ the official tower variant
+# (page A's comparison table: RMSNorm and SwiGLU; Step 3: [h*f, w*f] angles with the
+# half-vector rotation; Step 1 item 6: pixels to [-1, 1])
+
+def test_rms_norm_closed_forms():
+    g = np.full(1024, 1.0, F32)
+    for c in (0.375, -2.0, 13.0):
+        y = O.rms_norm(np.full((1, 1024), c, F32), g, 1e-6)
+        assert np.allclose(y, np.sign(c) * abs(c) / math.sqrt(c * c + 1e-6), rtol=1e-6)
+    x = np.random.default_rng(41).standard_normal((4, 1024)).astype(F32) * 3
+    y = O.rms_norm(x, g, 1e-6)
+    assert np.allclose((y * y).mean(axis=1), 1.0, rtol=1e-5)                 # unit mean square
+    assert np.allclose(O.rms_norm(8 * x, g, 1e-6), y, rtol=1e-5, atol=1e-6)  # scale invariance
+    gg = np.random.default_rng(42).standard_normal(1024).astype(F32)
+    assert np.allclose(O.rms_norm(x, gg, 1e-6), y * gg, rtol=1e-6)
+
+
+def test_silu_closed_forms():
+    z = np.array([0.0, math.log(3.0), -math.log(3.0), 30.0, -30.0, 1.7])
+    s = O.silu(z).astype(np.float64)
+    assert s[0] == 0.0
+    assert s[1] == pytest.approx(0.75 * math.log(3.0), rel=1e-7)           # sigma(ln 3) = 3/4
+    assert s[2] == pytest.approx(-0.25 * math.log(3.0), rel=1e-7)
+    assert s[3] == pytest.approx(30.0, rel=1e-7) and abs(s[4]) < 1e-11
+    w = np.linspace(-6, 6, 101)
+    assert np.allclose(O.silu(w) - O.silu(-w), w, atol=1e-6)                # silu(x) - silu(-x) = x
+
+
+def test_swiglu_hidden_selects_gate_and_up():
+    """One-hot gate row j and up row k: hidden = r(silu(y_j) * y_k)."""
+    F, D = 8, 16
+    cfg = dict(WL.MODEL, mlp=F, mlp_kind="swiglu")
+    rng = np.random.default_rng(43)
+    y = O.round_bf16(rng.standard_normal((5, D)).astype(F32))
+    w = np.zeros((2 * F, D), F32)
+    pairs = [(3, 7), (0, 0), (15, 2), (9, 9), (1, 14), (4, 5), (6, 11), (12, 8)]
+    for n, (j, k) in enumerate(pairs):
+        w[n, j] = 1.0
+        w[F + n, k] = 1.0
+    L = {"fc1_w": w, "fc1_b": np.zeros(2 * F, F32)}
+    h = O.mlp_hidden(y, L, cfg)
+    for n, (j, k) in enumerate(pairs):
+        assert np.array_equal(h[:, n], O.round_bf16(O.silu(y[:, j]) * y[:, k]))
+
+
+def test_rope_half_vector_pairs_and_angle_order():
+    """Dim i < 32 pairs with i + 32 and turns by the i-th angle of
+    [h*f0..h*f15, w*f0..w*f15] (page A, Step 3)."""
+    gy, gx = np.array([5]), np.array([11])
+    ang = O.rope_angles(gy, gx, 10000.0)[0]
+    for i in (0, 7, 15, 16, 23, 31):
+        v = np.zeros((1, 64), F32)
+        v[0, i] = 1.0
+        out = O.rope_half_vector(v, gy, gx, 10000.0)[0]
+        assert out[i] == pytest.approx(math.cos(ang[i]), abs=1e-6)
+        assert out[i + 32] == pytest.approx(math.sin(ang[i]), abs=1e-6)
+        assert np.count_nonzero(out) == 2
+        pos, f = (5, i) if i < 16 else (11, i - 16)
+        assert ang[i] == pytest.approx(pos * 10000.0 ** (-f / 16), rel=1e-12)
+
+
+def test_rope_pairings_differ_by_a_fixed_permutation():
+    """Swapping head dims 16..31 with 32..47 maps page A's pairing onto the
+    axis-halves pairing exactly, so q.k is the same under both when W_q, W_k
+    rows are permuted (the GPU applies the permutation to the weights)."""
+    perm = np.r_[0:16, 32:48, 16:32, 48:64]
+    rng = np.random.default_rng(44)
+    v = rng.standard_normal((9, 128)).astype(F32)
+    gy, gx = np.arange(9) % 3, np.arange(9) // 3 + 4
+    full = np.concatenate([perm + 64 * h for h in range(2)])
+    a = O.rope(v[:, full], gy, gx, 10000.0)
+    b = O.rope_half_vector(v, gy, gx, 10000.0)[:, full]
+    assert np.array_equal(a, b)
+
+
+def test_official_block_identity_with_zero_branches():
+    cfg = WL.MODEL_OFFICIAL
+    L = WL.make_weights_official(1)["layers"][0]
+    L = dict(L, proj_w=np.zeros_like(L["proj_w"]), proj_b=np.zeros_like(L["proj_b"]),
+             fc2_w=np.zeros_like(L["fc2_w"]), fc2_b=np.zeros_like(L["fc2_b"]))
+    x = O.round_bf16(np.random.default_rng(45).standard_normal((36, 1024)).astype(F32))
+    gy, gx = O.grid_positions(6, 6)
+    assert np.array_equal(O.vit_block(x, L, cfg, [36], gy, gx), x)

@@ -32,6 +32,13 @@ MODEL = dict(
     image_token_id=129264,
 )
 
+# The tower as the pages describe the released checkpoint (page A's comparison
+# table and Step 1 / Step 3): RMSNorm, SwiGLU MLP (gate and up of 4096 rows
+# each), pixels mapped to [-1, 1], and page A's RoPE pairing (angle vector
+# [h*f, w*f], dim i paired with dim i + 32).
+MODEL_OFFICIAL = dict(MODEL, norm="rmsnorm", mlp_kind="swiglu", rope_pairing="half_vector",
+                      mean=(0.5, 0.5, 0.5), std=(0.5, 0.5, 0.5))
+
 WEIGHT_SEED = 1000
 
 LAYER_KEYS = ("ln1_g", "ln1_b", "qkv_w", "qkv_b", "proj_w", "proj_b",
@@ -69,6 +76,20 @@ def make_layer(layer: int, seed: int = WEIGHT_SEED, hidden=1024, mlp=4096) -> di
         fc1_w=_normal(r, (mlp, hidden)), fc1_b=_normal(r, mlp),
         fc2_w=_normal(r, (hidden, mlp)), fc2_b=_normal(r, hidden),
     )
+
+
+def make_weights_official(n_layers: int, seed: int = WEIGHT_SEED) -> dict:
+    """Weights of MODEL_OFFICIAL: the default draws, with each layer's fc1
+    extended to the SwiGLU layout (rows [0, 4096) gate = the default fc1, rows
+    [4096, 8192) up, drawn from stream tag 500 + layer).  Norm betas are drawn
+    as usual and unused by RMSNorm."""
+    w = make_weights(n_layers, seed)
+    for l, L in enumerate(w["layers"]):
+        r = _rng(seed, 500 + l)
+        mlp, hidden = L["fc1_w"].shape
+        L["fc1_w"] = np.concatenate([L["fc1_w"], _normal(r, (mlp, hidden))])
+        L["fc1_b"] = np.concatenate([L["fc1_b"], _normal(r, mlp)])
+    return w
 
 
 def make_weights(n_layers: int, seed: int = WEIGHT_SEED) -> dict:

@@ -216,16 +216,49 @@ def run_reference(args):
     }), flush=True)
 
 
-def encode_flop(sizes, n_layers: int) -> int:
+def encode_flop(sizes, n_layers: int, swiglu: bool = False) -> int:
     """Algorithmic FLOPs of one encode of these images (unpadded K, full
-    bidirectional attention per image)."""
+    bidirectional attention per image; SwiGLU doubles the up-projection)."""
     tot = 0
+    fc1 = 8192 if swiglu else 4096
     for H, W in sizes:
         gh, gw = H // 14, W // 14
         n, t = gh * gw, ((gh + 2) // 3) * ((gw + 2) // 3)
         tot += 2 * n * 1024 * 588 + 2 * t * 5120 * 9216 + 2 * t * 5120 * 5120
-        tot += n_layers * (2 * n * 1024 * (3072 + 1024 + 4096 + 4096) + 4 * n * n * 64 * 16)
+        tot += n_layers * (2 * n * 1024 * (3072 + 1024 + fc1 + 4096) + 4 * n * n * 64 * 16)
     return tot
+
+
+def official_workload(pk, reps: int = 5):
+    """The released tower's block variant (RMSNorm, SwiGLU, half-vector RoPE
+    pairing, [-1, 1] pixels) on the 1344x1344 image at full depth: its own
+    weights (fc1 doubled for gate and up), CUDA events around the encode."""
+    import torch
+
+    import workloads as WL
+    import vit_vision_encoder_gb300 as dv
+    W = WL.make_weights_official(N_LAYERS)
+    enc = dv.Encoder(dv.weights_to_device(W), WL.MODEL_OFFICIAL)
+    img = torch.from_numpy(WL.workload_images(WORKLOAD)[0]).cuda()
+    out = torch.empty((N_TOK, 5120), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        enc.encode([img], out=out)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for r in range(reps):
+        enc.encode([img], out=out)
+        ev[r + 1].record()
+    torch.cuda.synchronize()
+    sec = statistics.mean(ev[r].elapsed_time(ev[r + 1]) / 1e3 for r in range(reps))
+    fl = encode_flop([(int(img.shape[0]), int(img.shape[1]))], N_LAYERS, swiglu=True)
+    if enc.status() != dv.OK:
+        raise RuntimeError("device status after the official variant")
+    enc.close()
+    return {"variant": "RMSNorm, SwiGLU (4096 gate + 4096 up), half-vector RoPE pairing, [-1, 1] pixels",
+            "image": [int(img.shape[0]), int(img.shape[1])], "layers": N_LAYERS, "tokens": N_TOK,
+            "ms_per_encode": round(sec * 1e3, 4), "tokens_per_s": round(N_TOK / sec, 1),
+            "tflops": round(fl / sec / 1e12, 1), "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3)}
 
 
 def other_workloads(dw, cfg, pk, reps: int = 5):
@@ -562,6 +595,7 @@ def main():
         line["workloads"] = other_workloads(dw, cfg, pk)
         line["preprocess"] = preprocess_workloads(pk)
         line["overlay_chunks"] = overlay_chunk_timing(pk)
+        line["official_variant"] = official_workload(pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

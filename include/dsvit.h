@@ -61,6 +61,8 @@ extern "C" {
 #define DS_VIT_EPI_BIAS_GELU 1   /* out = bf16(gelu_erf(a w^T + bias)) */
 #define DS_VIT_EPI_BIAS_RESID 2  /* out = bf16(out + (a w^T + bias))   (in place) */
 #define DS_VIT_EPI_QKV_ROPE 3    /* N = 3072: q, k rotated by 2D RoPE, then bf16 */
+#define DS_VIT_EPI_SWIGLU 4      /* N = 2F accumulators (w rows: F gate, F up) -> out [M, F] =
+                                    bf16(silu(gate + b_gate) * (up + b_up)) */
 
 /* Model constants.  Only hidden 1024, heads 16, head_dim 64, mlp 4096,
  * out_dim 5120, patch 14 and merge 3 are supported; n_layers 1..32. */
@@ -78,7 +80,22 @@ typedef struct ds_vit_config {
   float mean[3];         /* pixel mean per channel (CLIP) */
   float std[3];          /* pixel std per channel (CLIP) */
   int32_t image_token_id;
+  /* Block variant ([A] comparison table and Step 3 describe the released
+   * tower as RMSNorm + SwiGLU with the half-vector RoPE pairing). */
+  int32_t norm_kind;     /* DS_VIT_NORM_LAYER (gamma, beta) or DS_VIT_NORM_RMS (gamma; beta unused) */
+  int32_t mlp_kind;      /* DS_VIT_MLP_GELU or DS_VIT_MLP_SWIGLU (fc1 [2*mlp, hidden]: gate rows, then up rows) */
+  int32_t rope_pairing;  /* DS_VIT_ROPE_AXIS_HALVES or DS_VIT_ROPE_HALF_VECTOR */
 } ds_vit_config;
+
+#define DS_VIT_NORM_LAYER 0
+#define DS_VIT_NORM_RMS 1
+#define DS_VIT_MLP_GELU 0
+#define DS_VIT_MLP_SWIGLU 1
+/* per head: dims 0..31 rotated by the patch row and 32..63 by the patch column,
+ * each half as a rotate-half vector with pairs (j, j+16) */
+#define DS_VIT_ROPE_AXIS_HALVES 0
+/* per head: angle vector [row*f0..row*f15, col*f0..col*f15], dim i paired with i+32 */
+#define DS_VIT_ROPE_HALF_VECTOR 1
 
 /* One ViT block's weights: device bf16, nn.Linear layout [out, in]. */
 typedef struct ds_vit_layer_weights {
@@ -342,10 +359,16 @@ int ds_vit_device_status(const ds_vit_prepared* p, void* stream);
 int ds_vit_op_layernorm(const void* x, const void* g, const void* b, void* y, int64_t M,
                         float eps, void* stream);
 
+/* y = bf16(x * (1/sqrt(mean(x^2) + eps)) * g) over rows of 1024 (RMSNorm, the
+ * released tower's norm per [A]'s comparison table).  As ds_vit_op_layernorm. */
+int ds_vit_op_rmsnorm(const void* x, const void* g, void* y, int64_t M, float eps, void* stream);
+
 /* out[M, N] = epilogue(a[M, K] w[N, K]^T + bias[N]) on the tcgen05 tensor cores.
  * K % 64 == 0, N % 256 == 0, M >= 1.  For DS_VIT_EPI_QKV_ROPE: N = 3072,
  * rowpos (device int32 [M]) holds gy << 16 | gx of each row and rope_cs is the
- * table of ds_vit_op_rope_table; otherwise both may be NULL. */
+ * table of ds_vit_op_rope_table; otherwise both may be NULL.  For
+ * DS_VIT_EPI_SWIGLU, w and bias hold N/2 gate rows then N/2 up rows and out is
+ * [M, N/2]. */
 int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t N,
                      const void* bias, void* out, int32_t epilogue, const int32_t* rowpos,
                      const float* rope_cs, int32_t* status, void* stream);

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(_HERE, "libdsvit.so")
 
 OK, EINVAL, ERANGE, ECAP, ECUDA, ETIMEOUT, ENOMEM = 0, -1, -2, -3, -4, -5, -6
 TOK_START, TOK_IMAGE, TOK_NEWLINE, TOK_END = 0, 1, 2, 3
-EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESID, EPI_QKV_ROPE = 0, 1, 2, 3
+EPI_BIAS, EPI_BIAS_GELU, EPI_BIAS_RESID, EPI_QKV_ROPE, EPI_SWIGLU = 0, 1, 2, 3, 4
 MAX_LAYERS, MAX_IMAGES, MAX_PATCHES, MAX_TOKENS = 32, 64, 9216, 1024
 NOALLOC_MAX_PATCHES, NOALLOC_SCRATCH_BYTES = 1024, 21 * 1024 * 1024
 
@@ -33,7 +33,8 @@ class Config(C.Structure):
                 ("head_dim", C.c_int32), ("mlp", C.c_int32), ("out_dim", C.c_int32),
                 ("patch", C.c_int32), ("merge", C.c_int32), ("rope_theta", C.c_float),
                 ("ln_eps", C.c_float), ("mean", C.c_float * 3), ("std", C.c_float * 3),
-                ("image_token_id", C.c_int32)]
+                ("image_token_id", C.c_int32), ("norm_kind", C.c_int32), ("mlp_kind", C.c_int32),
+                ("rope_pairing", C.c_int32)]
 
 
 LAYER_FIELDS = ("ln1_g", "ln1_b", "qkv_w", "qkv_b", "proj_w", "proj_b",
@@ -84,6 +85,7 @@ SIGNATURES = {
     "ds_vit_device_status": (C.c_int, [_VP, _VP]),
     "ds_vit_set_kernel_timer": (C.c_int, [_VP, C.POINTER(_VP), _P_I32, _I32, _P_I32]),
     "ds_vit_op_layernorm": (C.c_int, [_VP, _VP, _VP, _VP, _I64, _F, _VP]),
+    "ds_vit_op_rmsnorm": (C.c_int, [_VP, _VP, _VP, _I64, _F, _VP]),
     "ds_vit_op_linear": (C.c_int, [_VP, _I64, _I32, _VP, _I32, _VP, _VP, _I32, _VP, _VP, _VP, _VP]),
     "ds_vit_op_rope_table": (C.c_int, [_VP, _I32, _F, _VP]),
     "ds_vit_op_attention": (C.c_int, [_VP, _P_I32, C.c_int, _VP, _VP, _VP]),
@@ -139,6 +141,9 @@ def make_config(model: dict, n_layers: int) -> Config:
     c.ln_eps = float(model["ln_eps"])
     c.mean = (C.c_float * 3)(*model["mean"])
     c.std = (C.c_float * 3)(*model["std"])
+    c.norm_kind = {"layernorm": 0, "rmsnorm": 1}[model.get("norm", "layernorm")]
+    c.mlp_kind = {"gelu": 0, "swiglu": 1}[model.get("mlp_kind", "gelu")]
+    c.rope_pairing = {"axis_halves": 0, "half_vector": 1}[model.get("rope_pairing", "axis_halves")]
     return c
 
 
@@ -351,6 +356,13 @@ def op_layernorm(x, g, b, eps=1e-6, out=None):
     return y
 
 
+def op_rmsnorm(x, g, eps=1e-6, out=None):
+    torch = _torch()
+    y = torch.empty_like(x) if out is None else out
+    check(lib.ds_vit_op_rmsnorm(_ptr(x), _ptr(g), _ptr(y), x.shape[0], eps, _stream()), "ds_vit_op_rmsnorm")
+    return y
+
+
 def op_rope_table(max_pos, theta=10000.0):
     torch = _torch()
     t = torch.empty((max_pos, 32), dtype=torch.float32, device="cuda")
@@ -363,7 +375,8 @@ def op_linear(a, w, bias, epilogue=EPI_BIAS, out=None, rowpos=None, rope_cs=None
     M, K = a.shape
     N = w.shape[0]
     if out is None:
-        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        n_out = N // 2 if epilogue == EPI_SWIGLU else N
+        out = torch.empty((M, n_out), dtype=torch.bfloat16, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda") if status is None else status
     check(lib.ds_vit_op_linear(_ptr(a), M, K, _ptr(w), N, _ptr(bias), _ptr(out), epilogue,
                                _ptr(rowpos), _ptr(rope_cs), _ptr(st), _stream()),

@@ -31,6 +31,7 @@ struct ds_vit_prepared {
   bf16* m1_perm;       // [5120, 9216], column p*1024 + c
   float* rope_cs;      // [kMaxPos, 32]
   bf16* pix_lut;       // [3, 256] normalised value of each (channel, byte)
+  bf16* qkv_perm;      // half-vector RoPE pairing: per layer W_qkv [3072, 1024] then b_qkv [3072]
   int* status;         // device status word
   WeightMap tm_patch, tm_m1, tm_m2;
   WeightMap tm_qkv[DS_VIT_MAX_LAYERS], tm_proj[DS_VIT_MAX_LAYERS];
@@ -43,6 +44,11 @@ struct ds_vit_prepared {
 };
 
 namespace {
+
+// Layer l of the permuted QKV copy: W [3072, 1024] at l * stride, b [3072] after it.
+constexpr size_t kQkvPermStride = size_t{3072} * 1025;
+bf16* qkv_perm_w(const ds_vit_prepared* p, int l) { return p->qkv_perm + l * kQkvPermStride; }
+bf16* qkv_perm_b(const ds_vit_prepared* p, int l) { return qkv_perm_w(p, l) + size_t{3072} * 1024; }
 
 constexpr int kMaxPos = DS_VIT_MAX_PATCHES;   // a grid side can reach 9216 (a 1 x 9216 grid)
 constexpr size_t kAlign = 256;
@@ -116,25 +122,32 @@ int check_config(const ds_vit_config* c) {
   if (!c) return DS_VIT_EINVAL;
   if (c->n_layers < 1 || c->n_layers > DS_VIT_MAX_LAYERS || c->hidden != 1024 || c->heads != 16 ||
       c->head_dim != 64 || c->mlp != 4096 || c->out_dim != 5120 || c->patch != 14 ||
-      c->merge != 3 || !(c->rope_theta > 0.f) || !(c->ln_eps > 0.f))
+      c->merge != 3 || !(c->rope_theta > 0.f) || !(c->ln_eps > 0.f) ||
+      (c->norm_kind != DS_VIT_NORM_LAYER && c->norm_kind != DS_VIT_NORM_RMS) ||
+      (c->mlp_kind != DS_VIT_MLP_GELU && c->mlp_kind != DS_VIT_MLP_SWIGLU) ||
+      (c->rope_pairing != DS_VIT_ROPE_AXIS_HALVES && c->rope_pairing != DS_VIT_ROPE_HALF_VECTOR))
     return DS_VIT_EINVAL;
   for (int i = 0; i < 3; ++i)
     if (!(c->std[i] != 0.f)) return DS_VIT_EINVAL;
   return DS_VIT_OK;
 }
 
-int check_weights(const ds_vit_weights* w, int n_layers) {
+// Every weight pointer non-null and 16-byte aligned; the norm betas may be
+// NULL under RMSNorm (unused there).
+int check_weights(const ds_vit_weights* w, int n_layers, bool rms) {
   if (!w) return DS_VIT_EINVAL;
-  const void* top[] = {w->patch_w, w->patch_b, w->lnm_g, w->lnm_b, w->m1_w,
-                       w->m1_b,    w->m2_w,    w->m2_b,  w->sentinel};
+  auto bad = [](const void* q, bool optional) { return q ? !aligned16(q) : !optional; };
+  const void* top[] = {w->patch_w, w->patch_b, w->lnm_g, w->m1_w, w->m1_b, w->m2_w, w->m2_b, w->sentinel};
   for (const void* q : top)
-    if (!q || !aligned16(q)) return DS_VIT_EINVAL;
+    if (bad(q, false)) return DS_VIT_EINVAL;
+  if (bad(w->lnm_b, rms)) return DS_VIT_EINVAL;
   for (int l = 0; l < n_layers; ++l) {
     const ds_vit_layer_weights& L = w->layers[l];
-    const void* lw[] = {L.ln1_g, L.ln1_b, L.qkv_w, L.qkv_b, L.proj_w, L.proj_b,
-                        L.ln2_g, L.ln2_b, L.fc1_w, L.fc1_b, L.fc2_w, L.fc2_b};
+    const void* lw[] = {L.ln1_g, L.qkv_w, L.qkv_b, L.proj_w, L.proj_b,
+                        L.ln2_g, L.fc1_w, L.fc1_b, L.fc2_w, L.fc2_b};
     for (const void* q : lw)
-      if (!q || !aligned16(q)) return DS_VIT_EINVAL;
+      if (bad(q, false)) return DS_VIT_EINVAL;
+    if (bad(L.ln1_b, rms) || bad(L.ln2_b, rms)) return DS_VIT_EINVAL;
   }
   return DS_VIT_OK;
 }
@@ -217,13 +230,17 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
              launch_gemm_agen(kAPixels, ag, p->tm_patch, tC_x, N, 1024, kPatchK,
                               static_cast<const bf16*>(w.patch_b), x, kEpiBias, p->status, st));
   if (dump_blocks) DSV_CUDA(cudaMemcpyAsync(dump_blocks, x, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
+  const bool rms = cfg.norm_kind == DS_VIT_NORM_RMS;
+  const bool swiglu = cfg.mlp_kind == DS_VIT_MLP_SWIGLU;
   for (int l = 0; l < cfg.n_layers; ++l) {
     const ds_vit_layer_weights& L = w.layers[l];
+    // The half-vector pairing runs on W_qkv / b_qkv with q, k rows permuted at preparation.
+    const bf16* qkv_b = p->qkv_perm ? qkv_perm_b(p, l) : static_cast<const bf16*>(L.qkv_b);
     DSV_LAUNCH(DS_VIT_KERNEL_LAYERNORM,
                launch_layernorm(x, static_cast<const bf16*>(L.ln1_g),
-                                static_cast<const bf16*>(L.ln1_b), y, N, cfg.ln_eps, st));
+                                static_cast<const bf16*>(L.ln1_b), y, N, cfg.ln_eps, st, rms));
     DSV_LAUNCH(DS_VIT_KERNEL_QKV_GEMM,
-               launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, 3072, 1024, static_cast<const bf16*>(L.qkv_b),
+               launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, 3072, 1024, qkv_b,
                            qkv, kEpiQkvRope, rowpos, p->rope_cs, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_ATTENTION, launch_attention(t_qkv, ab, o, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_PROJ_GEMM,
@@ -231,10 +248,11 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
                            x, kEpiBiasResid, nullptr, nullptr, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_LAYERNORM,
                launch_layernorm(x, static_cast<const bf16*>(L.ln2_g),
-                                static_cast<const bf16*>(L.ln2_b), y, N, cfg.ln_eps, st));
+                                static_cast<const bf16*>(L.ln2_b), y, N, cfg.ln_eps, st, rms));
     DSV_LAUNCH(DS_VIT_KERNEL_FC1_GEMM,
-               launch_gemm(tA_y, p->tm_fc1[l], tC_h, N, 4096, 1024, static_cast<const bf16*>(L.fc1_b), h,
-                           kEpiBiasGelu, nullptr, nullptr, p->status, st));
+               launch_gemm(tA_y, p->tm_fc1[l], tC_h, N, swiglu ? 8192 : 4096, 1024,
+                           static_cast<const bf16*>(L.fc1_b), h, swiglu ? kEpiSwiglu : kEpiBiasGelu, nullptr,
+                           nullptr, p->status, st));
     DSV_LAUNCH(DS_VIT_KERNEL_FC2_GEMM,
                launch_gemm(tA_h, p->tm_fc2[l], tC_x, N, 1024, 4096, static_cast<const bf16*>(L.fc2_b), x,
                            kEpiBiasResid, nullptr, nullptr, p->status, st));
@@ -244,7 +262,7 @@ int run_encode(const ds_vit_prepared* p, int n, const uint8_t* const* pix, const
   }
   DSV_LAUNCH(DS_VIT_KERNEL_LAYERNORM,
              launch_layernorm(x, static_cast<const bf16*>(w.lnm_g), static_cast<const bf16*>(w.lnm_b),
-                              y, N, cfg.ln_eps, st));
+                              y, N, cfg.ln_eps, st, rms));
   if (dump_final) DSV_CUDA(cudaMemcpyAsync(dump_final, y, N * 1024 * 2, cudaMemcpyDeviceToDevice, st));
   DSV_LAUNCH(DS_VIT_KERNEL_MERGER_GEMM1,
              launch_gemm_agen(kAMerge, ag, p->tm_m1, tC_u, T, 5120, 9216,
@@ -323,7 +341,7 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w, ds_vit_pre
   if (!out) return DS_VIT_EINVAL;
   *out = nullptr;
   DSV_TRY(check_config(cfg));
-  DSV_TRY(check_weights(w, cfg->n_layers));
+  DSV_TRY(check_weights(w, cfg->n_layers, cfg->norm_kind == DS_VIT_NORM_RMS));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   ds_vit_prepared* p = new (std::nothrow) ds_vit_prepared();
   if (!p) return DS_VIT_ENOMEM;
@@ -354,15 +372,25 @@ int ds_vit_prepare(const ds_vit_config* cfg, const ds_vit_weights* w, ds_vit_pre
     }
     rc = launch_pixel_lut(norm, p->pix_lut, st);
   }
+  if (rc == DS_VIT_OK && cfg->rope_pairing == DS_VIT_ROPE_HALF_VECTOR) {
+    if (cudaMalloc(&p->qkv_perm, static_cast<size_t>(cfg->n_layers) * kQkvPermStride * 2) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(DS_VIT_ENOMEM);
+    }
+    for (int l = 0; rc == DS_VIT_OK && l < cfg->n_layers; ++l)
+      rc = launch_permute_qk_rows(static_cast<const bf16*>(w->layers[l].qkv_w),
+                                  static_cast<const bf16*>(w->layers[l].qkv_b), qkv_perm_w(p, l),
+                                  qkv_perm_b(p, l), 1024, 1024, st);
+  }
   if (rc != DS_VIT_OK) return fail(rc);
   bool ok = make_weight_map(&p->tm_patch, p->patch_w_pad, 1024, kPatchK) &&
             make_weight_map(&p->tm_m1, p->m1_perm, 5120, 9216) &&
             make_weight_map(&p->tm_m2, w->m2_w, 5120, 5120);
   for (int l = 0; ok && l < cfg->n_layers; ++l) {
     const ds_vit_layer_weights& L = w->layers[l];
-    ok = make_weight_map(&p->tm_qkv[l], L.qkv_w, 3072, 1024) &&
+    ok = make_weight_map(&p->tm_qkv[l], p->qkv_perm ? qkv_perm_w(p, l) : L.qkv_w, 3072, 1024) &&
          make_weight_map(&p->tm_proj[l], L.proj_w, 1024, 1024) &&
-         make_weight_map(&p->tm_fc1[l], L.fc1_w, 4096, 1024) &&
+         make_weight_map(&p->tm_fc1[l], L.fc1_w, cfg->mlp_kind == DS_VIT_MLP_SWIGLU ? 8192 : 4096, 1024) &&
          make_weight_map(&p->tm_fc2[l], L.fc2_w, 1024, 4096);
   }
   if (!ok) return fail(DS_VIT_ECUDA);
@@ -380,6 +408,7 @@ int ds_vit_release(ds_vit_prepared* p) {
   cudaFree(p->patch_w_pad);
   cudaFree(p->m1_perm);
   cudaFree(p->rope_cs);
+  cudaFree(p->qkv_perm);
   cudaFree(p->pix_lut);
   cudaFree(p->status);
   delete p;
@@ -546,18 +575,25 @@ int ds_vit_op_layernorm(const void* x, const void* g, const void* b, void* y, in
                           static_cast<cudaStream_t>(stream));
 }
 
+int ds_vit_op_rmsnorm(const void* x, const void* g, void* y, int64_t M, float eps, void* stream) {
+  if (!x || !g || !y || M < 0 || !(eps > 0.f)) return DS_VIT_EINVAL;
+  if (!aligned16(x) || !aligned16(g) || !aligned16(y) || x == y) return DS_VIT_EINVAL;
+  return launch_layernorm(static_cast<const bf16*>(x), static_cast<const bf16*>(g), nullptr,
+                          static_cast<bf16*>(y), M, eps, static_cast<cudaStream_t>(stream), true);
+}
+
 int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t N, const void* bias,
                      void* out, int32_t epilogue, const int32_t* rowpos, const float* rope_cs,
                      int32_t* status, void* stream) {
   if (!a || !w || !bias || !out || !status || M < 1 || M > INT32_MAX || K < 64 || K % 64 != 0 ||
-      N < 256 || N % 256 != 0 || epilogue < 0 || epilogue > 3)
+      N < 256 || N % 256 != 0 || epilogue < 0 || epilogue > 4)
     return DS_VIT_EINVAL;
   if (epilogue == kEpiQkvRope && (N != 3072 || !rowpos || !rope_cs)) return DS_VIT_EINVAL;
   if (!aligned16(a) || !aligned16(w) || !aligned16(bias) || !aligned16(out)) return DS_VIT_EINVAL;
   CUtensorMap tA, tC;
   WeightMap tB;
   if (!make_tmap_bf16(&tA, a, M, K, 128) || !make_weight_map(&tB, w, N, K) ||
-      !make_tmap_store_bf16(&tC, out, M, N))
+      !make_tmap_store_bf16(&tC, out, M, epilogue == kEpiSwiglu ? N / 2 : N))
     return DS_VIT_ECUDA;
   return launch_gemm(tA, tB, tC, static_cast<int>(M), N, K, static_cast<const bf16*>(bias),
                      static_cast<bf16*>(out), epilogue, rowpos, rope_cs, status,

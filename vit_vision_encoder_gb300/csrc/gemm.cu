@@ -420,7 +420,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
           mbar_expect_tx(full_bar(stage), ASRC == kATma ? C::STAGE_BYTES : C::B_BYTES);
           if constexpr (ASRC == kATma)
             tma_load_2d(stage_a(stage), &tmA, full_bar(stage), kb * C::BK, mb * C::BM);
-          tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
+          if constexpr (EPI == kEpiSwiglu) {
+            // Gate rows nb*128.. and the matching up rows N/2 + nb*128.. fill
+            // the two halves of the B stage (128-row boxes).
+            tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * (BN / 2));
+            tma_load_2d(stage_b(stage) + (BN / 2) * C::BK * 2, &tmB, full_bar(stage), kb * C::BK,
+                        p.N / 2 + nb * (BN / 2));
+          } else {
+            tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
+          }
           ++issued_fills;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -508,7 +516,11 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
       if (warp == 0) {
 #pragma unroll
         for (int q = lane; q < BN / 8; q += 32) {
-          const uint4 b = __ldg(reinterpret_cast<const uint4*>(p.bias + nb * BN) + q);
+          // SwiGLU: gate biases in the first half of the buffer, up biases in the second.
+          const bf16* bsrc = EPI == kEpiSwiglu
+                                 ? (q < BN / 16 ? p.bias + nb * (BN / 2) : p.bias + p.N / 2 + nb * (BN / 2) - BN / 2)
+                                 : p.bias + nb * BN;
+          const uint4 b = __ldg(reinterpret_cast<const uint4*>(bsrc) + q);
           asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bias_buf + q * 16), "r"(b.x),
                        "r"(b.y), "r"(b.z), "r"(b.w)
                        : "memory");
@@ -553,19 +565,23 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
       }
       if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
       tc_fence_after();
+      // Output chunks of 32 columns per warp; SwiGLU tiles output BN/2 columns.
+      constexpr int kChunks = EPI == kEpiSwiglu ? BN / 128 : BN / 64;
 #pragma unroll
-      for (int cc = 0; cc < BN / 64; ++cc) {
+      for (int cc = 0; cc < kChunks; ++cc) {
         const int c = 2 * cc + grp;
-        const int n0 = nb * BN + c * 32;
+        const int n0 = (EPI == kEpiSwiglu ? nb * (BN / 2) : nb * BN) + c * 32;
         uint4 rx[4];
         if constexpr (EPI == kEpiBiasResid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) rx[q] = rxa[cc][q];
         }
         uint32_t r[32];
+        uint32_t ru[EPI == kEpiSwiglu ? 32 : 1];
         tmem_ld32(tmem_base + acc * BN + c * 32 + lane_sel, r);
+        if constexpr (EPI == kEpiSwiglu) tmem_ld32(tmem_base + acc * BN + BN / 2 + c * 32 + lane_sel, ru);
         tmem_wait_ld();
-        if (cc == BN / 64 - 1) {
+        if (cc == kChunks - 1) {
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(tempty_bar(acc));
@@ -586,6 +602,25 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
         if constexpr (EPI == kEpiBiasGelu) {
 #pragma unroll
           for (int i = 0; i < 32; i += 2) gelu_erf2(v[i], v[i + 1]);
+        } else if constexpr (EPI == kEpiSwiglu) {
+          // v = gate + b_gate; out = silu(v) * (up + b_up), silu(v) = v / (1 + 2^(-v log2 e)).
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t bw[4];
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
+                         : "r"(bias_buf + BN + c * 64 + q * 16));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+#pragma unroll
+              for (int hh = 0; hh < 2; ++hh) {
+                const int i = q * 8 + 2 * e + hh;
+                const float u = __fadd_rn(__uint_as_float(ru[i]), hh ? bf16hi(bw[e]) : bf16lo(bw[e]));
+                const float den = __fadd_rn(1.f, ex2_approx(__fmul_rn(v[i], -1.4426950408889634f)));
+                v[i] = __fmul_rn(__fmul_rn(v[i], rcp_approx(den)), u);
+              }
+            }
+          }
         } else if constexpr (EPI == kEpiBiasResid) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -734,6 +769,8 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
   GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status, tile_order(M, K)};
+  // SwiGLU pairs the gate and up halves of one 256-column tile (two 128-row B boxes).
+  if (epi == kEpiSwiglu) return launch_gemm_t<256, kEpiSwiglu>(tmA, B.bn128, tmC, p, stream);
   if (gemm_bn(M, N) == 128) {
     const CUtensorMap& tmB = B.bn128;
     switch (epi) {

@@ -34,7 +34,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Epilogue kinds of the tcgen05 GEMM (same values as DS_VIT_EPI_*).
-enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3 };
+enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3, kEpiSwiglu = 4 };
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 // Row-major bf16 matrix [rows, cols], box [box_rows, 64 cols], 128-byte swizzle,
@@ -79,7 +79,12 @@ int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* ou
                      cudaStream_t stream);
 
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
-                     cudaStream_t stream);
+                     cudaStream_t stream, bool rms = false);
+
+// W'[r] = W[swap(r)], b'[r] = b[swap(r)] for the q and k rows (r < 2 hidden),
+// swap exchanging head dims 16..31 and 32..47; v rows copied.  [3 hidden, K].
+int launch_permute_qk_rows(const bf16* w, const bf16* b, bf16* w_perm, bf16* b_perm, int hidden, int K,
+                           cudaStream_t stream);
 
 struct ImageBatch {
   int n;

@@ -15,6 +15,9 @@ namespace {
 // the biased variance of the centred values; y = (x - mu) * (1/sqrt(var + eps))
 // * g + b rounded to bf16 ("Step 2": the final-norm boundary; block pre-norms).
 // gamma and beta are read after the statistics (they are hot in L1/L2).
+// RMS mode (RMSNorm, page A's comparison table for the released tower): no
+// centring and no beta, y = x * (1/sqrt(mean(x^2) + eps)) * g.
+template <bool RMS>
 __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ x,
                                                         const bf16* __restrict__ g,
                                                         const bf16* __restrict__ b,
@@ -35,16 +38,19 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
     xw[4 * q + 2] = u.z;
     xw[4 * q + 3] = u.w;
   }
-  float s0 = 0.f, s1 = 0.f;
+  float mu = 0.f;
+  if constexpr (!RMS) {
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    s0 += bf16lo(xw[i]);
-    s1 += bf16hi(xw[i]);
+    for (int i = 0; i < 16; ++i) {
+      s0 += bf16lo(xw[i]);
+      s1 += bf16hi(xw[i]);
+    }
+    float s = s0 + s1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
+    mu = __fdiv_rn(s, 1024.f);
   }
-  float s = s0 + s1;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-  const float mu = __fdiv_rn(s, 1024.f);
   float q0 = 0.f, q1 = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -61,17 +67,22 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   uint4* yr = reinterpret_cast<uint4*>(y + row * 1024);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const uint4 gu = __ldg(g4 + q * 32 + lane), bu = __ldg(b4 + q * 32 + lane);
+    const uint4 gu = __ldg(g4 + q * 32 + lane);
+    const uint4 bu = RMS ? make_uint4(0, 0, 0, 0) : __ldg(b4 + q * 32 + lane);
     const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
     const uint32_t bw[4] = {bu.x, bu.y, bu.z, bu.w};
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const uint32_t w = xw[4 * q + e];
-      const float y0 =
-          __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16lo(w), mu), inv), bf16lo(gw[e])), bf16lo(bw[e]));
-      const float y1 =
-          __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16hi(w), mu), inv), bf16hi(gw[e])), bf16hi(bw[e]));
+      float y0, y1;
+      if constexpr (RMS) {
+        y0 = __fmul_rn(__fmul_rn(bf16lo(w), inv), bf16lo(gw[e]));
+        y1 = __fmul_rn(__fmul_rn(bf16hi(w), inv), bf16hi(gw[e]));
+      } else {
+        y0 = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16lo(w), mu), inv), bf16lo(gw[e])), bf16lo(bw[e]));
+        y1 = __fadd_rn(__fmul_rn(__fmul_rn(__fsub_rn(bf16hi(w), mu), inv), bf16hi(gw[e])), bf16hi(bw[e]));
+      }
       o[e] = pack_bf16x2(y0, y1);
     }
     yr[q * 32 + lane] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -101,6 +112,24 @@ __global__ void rope_table_kernel(float* table, int max_pos, double theta) {
   const double a = static_cast<double>(pos) * f;
   table[pos * 32 + i] = static_cast<float>(cos(a));
   table[pos * 32 + 16 + i] = static_cast<float>(sin(a));
+}
+
+// q and k rows of W_qkv (and b_qkv) with head dims 16..31 and 32..47 swapped:
+// the half-vector pairing (dim i with i + 32, angles [row f, col f]) becomes
+// the axis-halves pairing the QKV epilogue applies, and q.k is unchanged
+// because q and k take the same permutation.  One block per output row.
+__global__ void permute_qk_rows_kernel(const bf16* __restrict__ w, const bf16* __restrict__ b,
+                                       bf16* __restrict__ wp, bf16* __restrict__ bp, int hidden, int K) {
+  const int r = blockIdx.x;                     // destination row
+  int src = r;
+  if (r < 2 * hidden) {
+    const int d = r % 64, base = r - d;
+    const int sd = (d >= 16 && d < 32) ? d + 16 : ((d >= 32 && d < 48) ? d - 16 : d);
+    src = base + sd;
+  }
+  for (int k = threadIdx.x; k < K; k += blockDim.x)
+    wp[static_cast<int64_t>(r) * K + k] = w[static_cast<int64_t>(src) * K + k];
+  if (threadIdx.x == 0) bp[r] = b[src];
 }
 
 __global__ void permute_m1_kernel(const bf16* __restrict__ w, bf16* __restrict__ wp) {
@@ -202,10 +231,11 @@ __global__ void __launch_bounds__(128) overlay_chunk_kernel(bf16* __restrict__ c
 }  // namespace
 
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
-                     cudaStream_t stream) {
+                     cudaStream_t stream, bool rms) {
   if (M <= 0) return DS_VIT_OK;
-  const cudaError_t e = launch_pdl(layernorm_kernel, dim3(static_cast<unsigned>((M + 3) / 4)), dim3(128), 0,
-                                   stream, x, g, b, y, M, eps);
+  const dim3 grid(static_cast<unsigned>((M + 3) / 4));
+  const cudaError_t e = rms ? launch_pdl(layernorm_kernel<true>, grid, dim3(128), 0, stream, x, g, b, y, M, eps)
+                            : launch_pdl(layernorm_kernel<false>, grid, dim3(128), 0, stream, x, g, b, y, M, eps);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
@@ -218,6 +248,12 @@ int launch_pixel_lut(const PixelNorm& norm, bf16* lut, cudaStream_t stream) {
 int launch_rope_table(float* table, int max_pos, float theta, cudaStream_t stream) {
   const int n = max_pos * 16;
   rope_table_kernel<<<(n + 255) / 256, 256, 0, stream>>>(table, max_pos, static_cast<double>(theta));
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_permute_qk_rows(const bf16* w, const bf16* b, bf16* w_perm, bf16* b_perm, int hidden, int K,
+                           cudaStream_t stream) {
+  permute_qk_rows_kernel<<<3 * hidden, 256, 0, stream>>>(w, b, w_perm, b_perm, hidden, K);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 

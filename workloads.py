@@ -92,6 +92,45 @@ def make_weights_official(n_layers: int, seed: int = WEIGHT_SEED) -> dict:
     return w
 
 
+# The Qwen3-VL-style tower (page A's comparison table; oracle/qwen.py lists the
+# readings): hidden 1152, 16 heads of 72, MLP 4608, 27 layers, 16x16x2
+# patches, 48x48 position table, 2x2 merger to 5120, DeepStack taps 8/16/24.
+QWEN_MODEL = dict(hidden=1152, heads=16, head_dim=72, mlp=4608, out_dim=5120, patch=16, temporal=2,
+                  merge=2, pos_side=48, rope_theta=10000.0, ln_eps=1e-6, taps=(8, 16, 24),
+                  n_layers=27, mean=MODEL["mean"], std=MODEL["std"])
+QWEN_SEED = 2000
+
+
+def _qwen_merger(r, D=1152, out=5120):
+    return dict(ln_g=_normal(r, D, mean=1.0), ln_b=_normal(r, D), w1=_normal(r, (4 * D, 4 * D)),
+                b1=_normal(r, 4 * D), w2=_normal(r, (out, 4 * D)), b2=_normal(r, out))
+
+
+def make_weights_qwen(n_layers: int, seed: int = QWEN_SEED) -> dict:
+    """bf16 bit patterns: patch_w [1152, 1536] (column ((c*2 + t)*16 + y)*16 + x),
+    pos_table [48*48, 1152] (row y*48 + x), per layer the fields of a block
+    (qkv_w [3456, 1152], fc1_w [4608, 1152], ...), "merger" and three
+    "deepstack" mergers (ln_g, ln_b, w1 [4608, 4608], b1, w2 [5120, 4608], b2).
+    Stream tags: 0 patch/pos, 1 + l layer l, 100 merger, 101..103 DeepStack."""
+    D, F = 1152, 4608
+    r0 = _rng(seed, 0)
+    w = dict(patch_w=_normal(r0, (D, 1536)), patch_b=_normal(r0, D), pos_table=_normal(r0, (48 * 48, D)))
+    layers = []
+    for l in range(n_layers):
+        r = _rng(seed, 1 + l)
+        layers.append(dict(
+            ln1_g=_normal(r, D, mean=1.0), ln1_b=_normal(r, D),
+            qkv_w=_normal(r, (3 * D, D)), qkv_b=_normal(r, 3 * D),
+            proj_w=_normal(r, (D, D)), proj_b=_normal(r, D),
+            ln2_g=_normal(r, D, mean=1.0), ln2_b=_normal(r, D),
+            fc1_w=_normal(r, (F, D)), fc1_b=_normal(r, F),
+            fc2_w=_normal(r, (D, F)), fc2_b=_normal(r, D)))
+    w["layers"] = layers
+    w["merger"] = _qwen_merger(_rng(seed, 100))
+    w["deepstack"] = [_qwen_merger(_rng(seed, 101 + i)) for i in range(3)]
+    return w
+
+
 def make_weights(n_layers: int, seed: int = WEIGHT_SEED) -> dict:
     """All weights as bf16 bit patterns (uint16), nn.Linear layout [out, in].
 

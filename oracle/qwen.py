@@ -69,9 +69,10 @@ def patch_order(gh: int, gw: int):
 
 
 def patchify(img: np.ndarray, mean, std) -> np.ndarray:
-    """uint8 [H, W, 3] (H, W multiples of 32) -> normalised fp32 [N, 1536],
-    rows in merge-group order, column ((c*2 + t)*16 + y)*16 + x, both temporal
-    slots holding the same frame."""
+    """uint8 [H, W, 3] (H, W multiples of 32) -> normalised bf16 values [N, 1536]
+    (r((p/255 - mean_c)/std_c), fp32 arithmetic: the patch matrix is a stored
+    tensor), rows in merge-group order, column ((c*2 + t)*16 + y)*16 + x, both
+    temporal slots holding the same frame."""
     H, W = img.shape[:2]
     gh, gw = H // 16, W // 16
     gy, gx = patch_order(gh, gw)
@@ -80,7 +81,7 @@ def patchify(img: np.ndarray, mean, std) -> np.ndarray:
     for r, (y, x) in enumerate(zip(gy, gx)):
         p = px[16 * y:16 * y + 16, 16 * x:16 * x + 16, :].transpose(2, 0, 1)            # [c, y, x]
         out[r] = np.stack([p, p], axis=1).reshape(-1)                                    # [c, t, y, x]
-    return out
+    return round_bf16(out)
 
 
 def pos_interp(table: np.ndarray, gh: int, gw: int) -> np.ndarray:

@@ -229,6 +229,42 @@ def encode_flop(sizes, n_layers: int, swiglu: bool = False) -> int:
     return tot
 
 
+def qwen_workload(pk, reps: int = 5, H: int = 1024, W: int = 1024):
+    """The Qwen3-VL-style tower (27 blocks, hidden 1152, 16 heads of 72, 2x2
+    merger, three DeepStack mergers) on a 1024x1024 image (4096 patches, 1024
+    tokens): CUDA events around ds_vit_qwen_encode with all four outputs.
+    Algorithmic FLOPs count the real head width (72), not the padding."""
+    import torch
+
+    import workloads as WL
+    import vit_vision_encoder_gb300 as dv
+    cfg = WL.QWEN_MODEL
+    Wq = WL.make_weights_qwen(cfg["n_layers"])
+    enc = dv.QwenEncoder(dv.weights_to_device(Wq), cfg)
+    img = torch.from_numpy(WL.uniform_image(H, W, seed=8)).cuda()
+    T, N = (H // 32) * (W // 32), (H // 16) * (W // 16)
+    out = torch.empty((T, 5120), dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):
+        enc.encode(img, out=out)
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    ev[0].record()
+    for r in range(reps):
+        enc.encode(img, out=out)
+        ev[r + 1].record()
+    torch.cuda.synchronize()
+    sec = statistics.mean(ev[r].elapsed_time(ev[r + 1]) / 1e3 for r in range(reps))
+    L = cfg["n_layers"]
+    fl = 2 * N * 1152 * 1536 + L * (2 * N * 1152 * (3456 + 1152 + 4608 + 4608) + 4 * N * N * 72 * 16)
+    fl += 4 * (2 * T * 4608 * 4608 + 2 * T * 5120 * 4608)
+    enc.close()
+    return {"tower": "Qwen3-VL-style: 16x16x2 patches, 27 blocks of 1152 (16 heads of 72), 2x2 merger + 3 DeepStack",
+            "image": [H, W], "patches": N, "tokens": T, "ms_per_encode": round(sec * 1e3, 4),
+            "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
+            "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3),
+            "note": "heads padded to 128 in the QKV projection and attention tiles; FLOPs counted at 72"}
+
+
 def official_workload(pk, reps: int = 5):
     """The released tower's block variant (RMSNorm, SwiGLU, half-vector RoPE
     pairing, [-1, 1] pixels) on the 1344x1344 image at full depth: its own
@@ -596,6 +632,7 @@ def main():
         line["preprocess"] = preprocess_workloads(pk)
         line["overlay_chunks"] = overlay_chunk_timing(pk)
         line["official_variant"] = official_workload(pk)
+        line["qwen_tower"] = qwen_workload(pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:

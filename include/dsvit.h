@@ -344,6 +344,74 @@ int ds_vit_overlay_chunk(void* chunk, int64_t chunk_begin, int64_t chunk_rows, i
 int ds_vit_set_kernel_timer(ds_vit_prepared* p, void* const* events, int32_t* kinds,
                             int32_t n_slots, int32_t* n_recorded);
 
+/* ---------------------------------------------------------------------------
+ * The Qwen3-VL-style tower ([A] comparison table, "Patch order reflects the
+ * spatial reducer", "Qwen3-VL has two layers of positional meaning",
+ * "DeepStack means that 'vision output' is plural"): 16x16x2 patches (a still
+ * image fills both temporal slots) in 2x2-merge-group order, a learned 48x48
+ * position table interpolated (bilinear, align corners) to the grid, n_layers
+ * pre-LayerNorm blocks (hidden 1152, 16 heads of 72, 2D RoPE: dims 0..35 at
+ * the patch row and 36..71 at the column, pairs (j, j+18), GELU MLP 4608), a
+ * 2x2 merger (LayerNorm, 4 rows -> 4608, Linear 4608 + GELU, Linear 5120), and
+ * three DeepStack mergers of the same shape on the outputs of blocks 8, 16, 24.
+ * Config: hidden 1152, heads 16, head_dim 72, mlp 4608, out_dim 5120, patch
+ * 16, merge 2, norm_kind LAYER, mlp_kind GELU (DS_VIT_EINVAL otherwise).
+ * ------------------------------------------------------------------------- */
+typedef struct ds_vit_qwen_merger {
+  const void *ln_g, *ln_b;   /* [1152] */
+  const void *w1, *b1;       /* [4608, 4608] (input = 4 patch rows concatenated), [4608] */
+  const void *w2, *b2;       /* [5120, 4608], [5120] */
+} ds_vit_qwen_merger;
+
+typedef struct ds_vit_qwen_weights {
+  const void* patch_w;       /* [1152, 1536], column ((c*2 + t)*16 + y)*16 + x */
+  const void* patch_b;       /* [1152] */
+  const void* pos_table;     /* [48*48, 1152], row y*48 + x */
+  ds_vit_layer_weights layers[DS_VIT_MAX_LAYERS];   /* qkv [3456, 1152] (q, k, v heads of 72), */
+                                                    /* proj [1152, 1152], fc1 [4608, 1152], fc2 [1152, 4608] */
+  ds_vit_qwen_merger merger;        /* primary output */
+  ds_vit_qwen_merger deepstack[3];  /* taps after blocks 8, 16, 24 (needed when n_layers reaches them) */
+} ds_vit_qwen_weights;
+
+typedef struct ds_vit_qwen_prepared ds_vit_qwen_prepared;
+
+/* Device copies (W_qkv with every head padded to 128 rows, the pixel table,
+ * the RoPE table) and TMA descriptors.  Synchronises `stream`. */
+int ds_vit_qwen_prepare(const ds_vit_config* cfg, const ds_vit_qwen_weights* w,
+                        ds_vit_qwen_prepared** out, void* stream);
+int ds_vit_qwen_release(ds_vit_qwen_prepared* p);
+
+/* Workspace of one H x W encode (host only).  H, W positive multiples of 32,
+ * T = (H/32)(W/32) <= DS_VIT_MAX_TOKENS, grid sides <= 2048 (else
+ * DS_VIT_EINVAL / DS_VIT_ERANGE). */
+int ds_vit_qwen_workspace_bytes(int32_t H, int32_t W, size_t* bytes);
+
+/*
+ * ds_vit_qwen_encode: one image, device uint8 [H, W, 3] -> out device bf16
+ * [T, 5120] (merged tokens in merge-group = row-major order of the 2x2 grid)
+ * and, when `deepstack` is not NULL, device bf16 [3, T, 5120] (taps 8, 16, 24;
+ * taps past n_layers are not written).  blocks (NULL to skip): device bf16
+ * [n_layers + 1, N, 1152], the patch embedding and each block's output, rows in
+ * merge-group order.  ws: device workspace of at least
+ * ds_vit_qwen_workspace_bytes.  Nothing is written on an argument error.
+ */
+int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int32_t H, int32_t W,
+                       void* out, void* deepstack, void* ws, size_t ws_bytes, void* blocks,
+                       void* stream);
+
+/*
+ * ds_vit_qwen_layout (host only): three-axis (t, h, w) M-RoPE positions of the
+ * span <vision_start>, h*w <image_pad>, <vision_end> that starts at sequence
+ * index seq_start, text before it holding positions equal to its indices
+ * ([A] "Qwen3-VL has two layers of positional meaning").  vision_start at
+ * p = seq_start on all axes; pad (y, x) at (p+1, p+1+y, p+1+x); vision_end at
+ * q = p+1+max(h, w); *rope_delta = q + 1 - (seq_start + h*w + 2), the offset
+ * that keeps later positions continuous.  pos: host int32 [3, h*w + 2] (axis
+ * major) with cap >= 3*(h*w + 2) entries, or NULL for rope_delta only.
+ */
+int ds_vit_qwen_layout(int32_t h, int32_t w, int32_t seq_start, int32_t* pos, int64_t cap,
+                       int32_t* rope_delta);
+
 /* Synchronise `stream`, then read and clear p's device status word: DS_VIT_OK,
  * or DS_VIT_ETIMEOUT if a kernel's bounded wait gave up since the last read. */
 int ds_vit_device_status(const ds_vit_prepared* p, void* stream);
@@ -364,7 +432,7 @@ int ds_vit_op_layernorm(const void* x, const void* g, const void* b, void* y, in
 int ds_vit_op_rmsnorm(const void* x, const void* g, void* y, int64_t M, float eps, void* stream);
 
 /* out[M, N] = epilogue(a[M, K] w[N, K]^T + bias[N]) on the tcgen05 tensor cores.
- * K % 64 == 0, N % 256 == 0, M >= 1.  For DS_VIT_EPI_QKV_ROPE: N = 3072,
+ * K % 64 == 0, N % 128 == 0 (N % 256 == 0 for SWIGLU), M >= 1.  For DS_VIT_EPI_QKV_ROPE: N = 3072,
  * rowpos (device int32 [M]) holds gy << 16 | gx of each row and rope_cs is the
  * table of ds_vit_op_rope_table; otherwise both may be NULL.  For
  * DS_VIT_EPI_SWIGLU, w and bias hold N/2 gate rows then N/2 up rows and out is

@@ -106,6 +106,22 @@ def test_plan_matches_oracle(dv):
             assert got[k] == ref[k], (H, W, k, got, ref)
 
 
+def test_qwen_layout_matches_oracle(dv):
+    import oracle.qwen as Q
+    for h, w, s in ((2, 3, 5), (32, 32, 0), (1, 1, 100), (5, 17, 12345), (64, 16, 7)):
+        pos, delta = dv.qwen_layout(h, w, s)
+        rp, rd = Q.layout(h, w, s)
+        assert np.array_equal(pos, rp) and delta == rd
+    b = C.c_int32(0)
+    assert dv.lib.ds_vit_qwen_layout(0, 3, 0, None, 0, C.byref(b)) == dv.EINVAL
+    small = np.zeros(5, np.int32)
+    assert dv.lib.ds_vit_qwen_layout(2, 3, 0, small.ctypes.data, 5, C.byref(b)) == dv.ECAP
+    n = C.c_size_t(0)
+    assert dv.lib.ds_vit_qwen_workspace_bytes(48, 64, C.byref(n)) == dv.EINVAL        # not a multiple of 32
+    assert dv.lib.ds_vit_qwen_workspace_bytes(1088, 1056, C.byref(n)) == dv.ERANGE    # 34 x 33 > 1024 tokens
+    assert dv.lib.ds_vit_qwen_workspace_bytes(1024, 1024, C.byref(n)) == dv.OK and n.value > 0
+
+
 def test_plan_and_preprocess_argument_checks(dv):
     L = dv.lib
     p = dv.Plan()

@@ -1,0 +1,97 @@
+"""The Qwen3-VL-style tower on the GPU (ds_vit_qwen_encode) against the
+oracle (oracle/qwen.py): every step recomputed from the GPU's own input to it
+(patch embedding with the interpolated position table, each block, the
+primary merger, the DeepStack merger of block 8) within the encode's step
+bound, and the free-running outputs within the oracle's own summation-order
+spread.  Grids: 2x2 merged (one partial query tile), 7x7 (ragged tiles),
+16x12; 9 blocks so that the first DeepStack tap is reached."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.qwen as Q
+import workloads as WL
+from gpu_util import COS_MIN, FLOOR_FACTOR, REL_TOL, assert_parity, bits_of, dev, host, rand_bits, rel_err, row_cos
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+N_LAYERS = 9
+
+
+@pytest.fixture(scope="module")
+def dv():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import vit_vision_encoder_gb300
+    return vit_vision_encoder_gb300
+
+
+@pytest.fixture(scope="module")
+def wq():
+    return WL.make_weights_qwen(N_LAYERS)
+
+
+@pytest.fixture(scope="module")
+def encq(dv, wq):
+    e = dv.QwenEncoder(dv.weights_to_device(wq), WL.QWEN_MODEL, n_layers=N_LAYERS)
+    yield e
+    e.close()
+
+
+def test_linear_width_1152(dv):
+    M, K, N = 777, 1152, 1152
+    a = rand_bits((M, K), 71)
+    w = rand_bits((N, K), 72, 1.0 / math.sqrt(K))
+    b = rand_bits(N, 73, 0.5)
+    x = rand_bits((M, N), 74)
+    ref = O.round_bf16(O.bits_to_f32(x) + (O.bits_to_f32(a) @ O.bits_to_f32(w).T + O.bits_to_f32(b)))
+    out = dev(x, torch)
+    y, st = dv.op_linear(dev(a, torch), dev(w, torch), dev(b, torch), dv.EPI_BIAS_RESID, out=out)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    e = rel_err(host(y), ref)
+    assert e.max() <= 1e-2
+
+
+@pytest.mark.parametrize("H,W", [(64, 64), (224, 224), (512, 384)])
+def test_qwen_encode(dv, encq, wq, H, W):
+    cfg = WL.QWEN_MODEL
+    img = WL.uniform_image(H, W, seed=300 + H)
+    out, deep, blocks = encq.encode(torch.from_numpy(img).cuda(), dump=True)
+    torch.cuda.synchronize()
+    bl = blocks.cpu()
+    gh, gw = H // 16, W // 16
+    gy, gx = Q.patch_order(gh, gw)
+    # patch embedding: r(r(pos) + A W^T + b)
+    A = Q.patchify(img, cfg["mean"], cfg["std"])
+    pos = Q.pos_interp(wq["pos_table"], gh, gw).reshape(gh, gw, -1)[gy, gx]
+    x0 = O.round_bf16(O.round_bf16(pos) + (O.mm(A, O.bits_to_f32(wq["patch_w"]).T) + O.bits_to_f32(wq["patch_b"])))
+    assert_parity(bits_of(bl[0]), x0, what="patch embedding")
+    for l in range(N_LAYERS):
+        ref = Q.block(bits_of(bl[l]), wq["layers"][l], cfg, gy, gx)
+        assert_parity(bits_of(bl[l + 1]), ref, what=f"block {l}")
+    assert_parity(host(out), Q.merger(bits_of(bl[N_LAYERS]), wq["merger"], cfg), what="merger")
+    assert_parity(host(deep[0]), Q.merger(bits_of(bl[8]), wq["deepstack"][0], cfg), what="deepstack 8")
+    # free-running outputs against the oracle, bounded by its own spread
+    ref_out, ref_deep = Q.encode(img, wq, cfg, n_layers=N_LAYERS)
+    with O.products("f64"):
+        alt_out, alt_deep = Q.encode(img, wq, cfg, n_layers=N_LAYERS)
+    for got, ref, alt, what in ((host(out), ref_out, alt_out, "primary"),
+                                (host(deep[0]), ref_deep[0], alt_deep[0], "deepstack 8")):
+        floor = rel_err(alt, ref)
+        e = rel_err(got, ref)
+        assert row_cos(got, ref).min() >= COS_MIN, what
+        assert e.max() <= max(REL_TOL, FLOOR_FACTOR * floor.max()), (what, e.max(), floor.max())
+        assert e.mean() <= max(REL_TOL / 10, FLOOR_FACTOR * floor.mean()), (what, e.mean())
+
+
+def test_qwen_rejects_bad_sizes(dv, encq):
+    img = torch.zeros((48, 64, 3), dtype=torch.uint8, device="cuda")
+    with pytest.raises(dv.DsVitError):
+        encq.encode(img)

@@ -57,6 +57,19 @@ class Span(C.Structure):
                 ("embed_row", C.c_int64)]
 
 
+MERGER_FIELDS = ("ln_g", "ln_b", "w1", "b1", "w2", "b2")
+
+
+class QwenMerger(C.Structure):
+    _fields_ = [(f, C.c_void_p) for f in MERGER_FIELDS]
+
+
+class QwenWeights(C.Structure):
+    _fields_ = ([("patch_w", C.c_void_p), ("patch_b", C.c_void_p), ("pos_table", C.c_void_p),
+                 ("layers", LayerWeights * MAX_LAYERS), ("merger", QwenMerger),
+                 ("deepstack", QwenMerger * 3)])
+
+
 class Plan(C.Structure):
     _fields_ = [(f, C.c_int32) for f in ("H", "W", "h", "w", "Hc", "Wc", "Hr", "Wr", "y0", "x0")]
 
@@ -90,6 +103,11 @@ SIGNATURES = {
     "ds_vit_op_rope_table": (C.c_int, [_VP, _I32, _F, _VP]),
     "ds_vit_op_attention": (C.c_int, [_VP, _P_I32, C.c_int, _VP, _VP, _VP]),
     "ds_vit_plan_image": (C.c_int, [_I32, _I32, C.POINTER(Plan)]),
+    "ds_vit_qwen_prepare": (C.c_int, [C.POINTER(Config), C.POINTER(QwenWeights), C.POINTER(_VP), _VP]),
+    "ds_vit_qwen_release": (C.c_int, [_VP]),
+    "ds_vit_qwen_workspace_bytes": (C.c_int, [_I32, _I32, C.POINTER(_SZ)]),
+    "ds_vit_qwen_encode": (C.c_int, [_VP, _VP, _I32, _I32, _VP, _VP, _VP, _SZ, _VP, _VP]),
+    "ds_vit_qwen_layout": (C.c_int, [_I32, _I32, _I32, _VP, _I64, _P_I32]),
     "ds_vit_preprocess_workspace_bytes": (C.c_int, [C.POINTER(Plan), C.POINTER(_SZ)]),
     "ds_vit_preprocess": (C.c_int, [C.POINTER(Plan), _VP, _VP, _VP, _SZ, _VP]),
 }
@@ -169,8 +187,12 @@ def weights_to_device(w: dict, device="cuda") -> dict:
     def up(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
 
-    out = {k: up(v) for k, v in w.items() if k != "layers"}
+    out = {k: up(v) for k, v in w.items() if k not in ("layers", "merger", "deepstack")}
     out["layers"] = [{k: up(v) for k, v in L.items()} for L in w["layers"]]
+    if "merger" in w:
+        out["merger"] = {k: up(v) for k, v in w["merger"].items()}
+    if "deepstack" in w:
+        out["deepstack"] = [{k: up(v) for k, v in M.items()} for M in w["deepstack"]]
     return out
 
 
@@ -294,6 +316,78 @@ class Encoder:
 
     def status(self) -> int:
         return lib.ds_vit_device_status(self.handle, _stream())
+
+
+class QwenEncoder:
+    """The Qwen3-VL-style tower (ds_vit_qwen_prepare) plus a cached workspace."""
+
+    def __init__(self, dev_weights: dict, model: dict, n_layers: int | None = None):
+        n_layers = len(dev_weights["layers"]) if n_layers is None else n_layers
+        self.n_layers = n_layers
+        self._keep = dev_weights
+        c = Config()
+        c.n_layers = n_layers
+        for k in ("hidden", "heads", "head_dim", "mlp", "out_dim", "patch", "merge"):
+            setattr(c, k, int(model[k]))
+        c.rope_theta, c.ln_eps = float(model["rope_theta"]), float(model["ln_eps"])
+        c.mean = (C.c_float * 3)(*model["mean"])
+        c.std = (C.c_float * 3)(*model["std"])
+        self.cfg = c
+        w = QwenWeights()
+        for k in ("patch_w", "patch_b", "pos_table"):
+            setattr(w, k, dev_weights[k].data_ptr())
+        for l in range(n_layers):
+            for k in LAYER_FIELDS:
+                setattr(w.layers[l], k, dev_weights["layers"][l][k].data_ptr())
+        for k in MERGER_FIELDS:
+            setattr(w.merger, k, dev_weights["merger"][k].data_ptr())
+        for t, M in enumerate(dev_weights.get("deepstack", [])):
+            for k in MERGER_FIELDS:
+                setattr(w.deepstack[t], k, M[k].data_ptr())
+        self._w = w
+        h = C.c_void_p()
+        check(lib.ds_vit_qwen_prepare(C.byref(c), C.byref(w), C.byref(h), _stream()), "ds_vit_qwen_prepare")
+        self.handle = h
+        self._ws = None
+
+    def close(self):
+        if self.handle:
+            lib.ds_vit_qwen_release(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def encode(self, img, out=None, deepstack=True, dump=False):
+        """uint8 CUDA tensor [H, W, 3] -> (out [T, 5120], deepstack [3, T, 5120] or
+        None, blocks [n_layers + 1, N, 1152] or None)."""
+        torch = _torch()
+        H, W = int(img.shape[0]), int(img.shape[1])
+        nb = C.c_size_t()
+        check(lib.ds_vit_qwen_workspace_bytes(H, W, C.byref(nb)), "ds_vit_qwen_workspace_bytes")
+        if self._ws is None or self._ws.numel() < nb.value:
+            self._ws = torch.empty(int(nb.value), dtype=torch.uint8, device="cuda")
+        T, N = (H // 32) * (W // 32), (H // 16) * (W // 16)
+        if out is None:
+            out = torch.empty((T, 5120), dtype=torch.bfloat16, device="cuda")
+        ds = torch.empty((3, T, 5120), dtype=torch.bfloat16, device="cuda") if deepstack else None
+        bl = torch.empty((self.n_layers + 1, N, 1152), dtype=torch.bfloat16, device="cuda") if dump else None
+        check(lib.ds_vit_qwen_encode(self.handle, _ptr(img), H, W, _ptr(out), _ptr(ds), _ptr(self._ws),
+                                     self._ws.numel(), _ptr(bl), _stream()), "ds_vit_qwen_encode")
+        return out, ds, bl
+
+
+def qwen_layout(h: int, w: int, seq_start: int):
+    """Three-axis M-RoPE positions [3, h*w + 2] of a Qwen image span and rope_delta."""
+    n = h * w + 2
+    pos = np.zeros((3, n), dtype=np.int32)
+    delta = C.c_int32()
+    check(lib.ds_vit_qwen_layout(h, w, seq_start, pos.ctypes.data, pos.size, C.byref(delta)),
+          "ds_vit_qwen_layout")
+    return pos, int(delta.value)
 
 
 def plan_image(H: int, W: int) -> dict:

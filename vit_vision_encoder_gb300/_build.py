@@ -10,7 +10,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsvit.so")
-SOURCES = ("api.cu", "gemm.cu", "attention.cu", "kernels.cu", "noalloc.cu", "preprocess.cu")
+SOURCES = ("api.cu", "gemm.cu", "attention.cu", "attention_qwen.cu", "kernels.cu", "noalloc.cu",
+           "preprocess.cu", "qwen.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr"]

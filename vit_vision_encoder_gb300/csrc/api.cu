@@ -586,7 +586,7 @@ int ds_vit_op_linear(const void* a, int64_t M, int32_t K, const void* w, int32_t
                      void* out, int32_t epilogue, const int32_t* rowpos, const float* rope_cs,
                      int32_t* status, void* stream) {
   if (!a || !w || !bias || !out || !status || M < 1 || M > INT32_MAX || K < 64 || K % 64 != 0 ||
-      N < 256 || N % 256 != 0 || epilogue < 0 || epilogue > 4)
+      N < 128 || N % 128 != 0 || epilogue < 0 || epilogue > 4)
     return DS_VIT_EINVAL;
   if (epilogue == kEpiQkvRope && (N != 3072 || !rowpos || !rope_cs)) return DS_VIT_EINVAL;
   if (!aligned16(a) || !aligned16(w) || !aligned16(bias) || !aligned16(out)) return DS_VIT_EINVAL;

@@ -767,11 +767,15 @@ bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k) {
 int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& tmC, int M, int N,
                 int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
-  if (M <= 0 || K <= 0 || K % 64 != 0 || N % 256 != 0) return DS_VIT_EINVAL;
+  if (M <= 0 || K <= 0 || K % 64 != 0 || N % 128 != 0) return DS_VIT_EINVAL;
   GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status, tile_order(M, K)};
   // SwiGLU pairs the gate and up halves of one 256-column tile (two 128-row B boxes).
-  if (epi == kEpiSwiglu) return launch_gemm_t<256, kEpiSwiglu>(tmA, B.bn128, tmC, p, stream);
-  if (gemm_bn(M, N) == 128) {
+  if (epi == kEpiSwiglu) {
+    if (N % 256 != 0) return DS_VIT_EINVAL;
+    return launch_gemm_t<256, kEpiSwiglu>(tmA, B.bn128, tmC, p, stream);
+  }
+  // Widths that are a multiple of 128 but not of 256 (1152) take 128-wide tiles.
+  if (N % 256 != 0 || gemm_bn(M, N) == 128) {
     const CUtensorMap& tmB = B.bn128;
     switch (epi) {
       case kEpiBias: return launch_gemm_t<128, kEpiBias>(tmA, tmB, tmC, p, stream);

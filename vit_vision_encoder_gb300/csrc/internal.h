@@ -78,8 +78,9 @@ struct AttnBatch {
 int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* out, int* status,
                      cudaStream_t stream);
 
+// Rows of `width` values: 1024 (LayerNorm or RMS) or 1152 (LayerNorm).
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
-                     cudaStream_t stream, bool rms = false);
+                     cudaStream_t stream, bool rms = false, int width = 1024);
 
 // W'[r] = W[swap(r)], b'[r] = b[swap(r)] for the q and k rows (r < 2 hidden),
 // swap exchanging head dims 16..31 and 32..47; v rows copied.  [3 hidden, K].

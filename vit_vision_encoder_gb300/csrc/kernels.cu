@@ -9,30 +9,34 @@ namespace dsvit {
 namespace {
 
 // ---------------------------------------------------------------- LayerNorm
-// One warp per 1024-wide row; each lane holds 32 values (four 16-byte loads,
-// coalesced across the warp), kept packed as bf16 pairs so a thread needs few
-// registers and many rows stay in flight per SM.  fp32 statistics: mean, then
-// the biased variance of the centred values; y = (x - mu) * (1/sqrt(var + eps))
-// * g + b rounded to bf16 ("Step 2": the final-norm boundary; block pre-norms).
-// gamma and beta are read after the statistics (they are hot in L1/L2).
+// One warp per row of W values (1024 for the encode, 1152 for the Qwen-style
+// tower); lane l holds the 16-byte chunks l, l+32, ... (coalesced across the
+// warp), kept packed as bf16 pairs so a thread needs few registers and many
+// rows stay in flight per SM.  fp32 statistics: mean, then the biased variance
+// of the centred values; y = (x - mu) * (1/sqrt(var + eps)) * g + b rounded to
+// bf16 ("Step 2": the final-norm boundary; block pre-norms).  gamma and beta
+// are read after the statistics (they are hot in L1/L2).
 // RMS mode (RMSNorm, page A's comparison table for the released tower): no
 // centring and no beta, y = x * (1/sqrt(mean(x^2) + eps)) * g.
-template <bool RMS>
+template <bool RMS, int W>
 __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__ x,
                                                         const bf16* __restrict__ g,
                                                         const bf16* __restrict__ b,
                                                         bf16* __restrict__ y, int64_t M,
                                                         float eps) {
+  constexpr int kChunks = W / 8;                  // 16-byte chunks per row
+  constexpr int kPerLane = (kChunks + 31) / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
   grid_dep_launch();
   grid_dep_wait();
   if (row >= M) return;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + row * 1024);
-  uint32_t xw[16];
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * W);
+  uint32_t xw[4 * kPerLane];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const uint4 u = __ldg(xr + q * 32 + lane);
+  for (int q = 0; q < kPerLane; ++q) {
+    const bool on = q * 32 + lane < kChunks;
+    const uint4 u = on ? __ldg(xr + q * 32 + lane) : make_uint4(0, 0, 0, 0);
     xw[4 * q] = u.x;
     xw[4 * q + 1] = u.y;
     xw[4 * q + 2] = u.z;
@@ -42,31 +46,37 @@ __global__ void __launch_bounds__(128) layernorm_kernel(const bf16* __restrict__
   if constexpr (!RMS) {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 4 * kPerLane; ++i) {
       s0 += bf16lo(xw[i]);
       s1 += bf16hi(xw[i]);
     }
     float s = s0 + s1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-    mu = __fdiv_rn(s, 1024.f);
+    mu = __fdiv_rn(s, static_cast<float>(W));
   }
   float q0 = 0.f, q1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float d0 = __fsub_rn(bf16lo(xw[i]), mu), d1 = __fsub_rn(bf16hi(xw[i]), mu);
-    q0 = __fmaf_rn(d0, d0, q0);
-    q1 = __fmaf_rn(d1, d1, q1);
+  for (int q = 0; q < kPerLane; ++q) {
+    if (q * 32 + lane < kChunks) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float d0 = __fsub_rn(bf16lo(xw[4 * q + e]), mu), d1 = __fsub_rn(bf16hi(xw[4 * q + e]), mu);
+        q0 = __fmaf_rn(d0, d0, q0);
+        q1 = __fmaf_rn(d1, d1, q1);
+      }
+    }
   }
   float ss = q0 + q1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
-  const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, 1024.f), eps)));
+  const float inv = __fdiv_rn(1.f, __fsqrt_rn(__fadd_rn(__fdiv_rn(ss, static_cast<float>(W)), eps)));
   const uint4* g4 = reinterpret_cast<const uint4*>(g);
   const uint4* b4 = reinterpret_cast<const uint4*>(b);
-  uint4* yr = reinterpret_cast<uint4*>(y + row * 1024);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * W);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kPerLane; ++q) {
+    if (q * 32 + lane >= kChunks) continue;
     const uint4 gu = __ldg(g4 + q * 32 + lane);
     const uint4 bu = RMS ? make_uint4(0, 0, 0, 0) : __ldg(b4 + q * 32 + lane);
     const uint32_t gw[4] = {gu.x, gu.y, gu.z, gu.w};
@@ -231,11 +241,17 @@ __global__ void __launch_bounds__(128) overlay_chunk_kernel(bf16* __restrict__ c
 }  // namespace
 
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
-                     cudaStream_t stream, bool rms) {
+                     cudaStream_t stream, bool rms, int width) {
   if (M <= 0) return DS_VIT_OK;
   const dim3 grid(static_cast<unsigned>((M + 3) / 4));
-  const cudaError_t e = rms ? launch_pdl(layernorm_kernel<true>, grid, dim3(128), 0, stream, x, g, b, y, M, eps)
-                            : launch_pdl(layernorm_kernel<false>, grid, dim3(128), 0, stream, x, g, b, y, M, eps);
+  cudaError_t e;
+  if (width == 1152)
+    e = launch_pdl(layernorm_kernel<false, 1152>, grid, dim3(128), 0, stream, x, g, b, y, M, eps);
+  else if (width != 1024)
+    return DS_VIT_EINVAL;
+  else
+    e = rms ? launch_pdl(layernorm_kernel<true, 1024>, grid, dim3(128), 0, stream, x, g, b, y, M, eps)
+            : launch_pdl(layernorm_kernel<false, 1024>, grid, dim3(128), 0, stream, x, g, b, y, M, eps);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }

@@ -440,6 +440,14 @@ def run_profile_case(case: str):
                                .view(np.int16)).cuda().view(torch.bfloat16)
         o = torch.empty((N_PATCH, 1024), dtype=torch.bfloat16, device="cuda")
         run = lambda: dv.op_attention(qkv, [N_PATCH], out=o)
+    elif case in ("qwen-encode", "qwen-attention"):
+        cfg = WL.QWEN_MODEL
+        n_layers = cfg["n_layers"] if case == "qwen-encode" else 1
+        Wq = WL.make_weights_qwen(n_layers)
+        enc = dv.QwenEncoder(dv.weights_to_device(Wq), cfg)
+        img = torch.from_numpy(WL.uniform_image(1024, 1024, seed=8)).cuda()
+        out = torch.empty((1024, 5120), dtype=torch.bfloat16, device="cuda")
+        run = lambda: enc.encode(img, out=out)
     elif case.startswith("gemm-"):
         K, N, epi = {"gemm-qkv": (1024, 3072, dv.EPI_BIAS), "gemm-fc1": (1024, 4096, dv.EPI_BIAS_GELU),
                      "gemm-fc2": (4096, 1024, dv.EPI_BIAS_RESID),

@@ -262,7 +262,7 @@ def qwen_workload(pk, reps: int = 5, H: int = 1024, W: int = 1024):
             "image": [H, W], "patches": N, "tokens": T, "ms_per_encode": round(sec * 1e3, 4),
             "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
             "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3),
-            "note": "heads padded to 128 in the QKV projection and attention tiles; FLOPs counted at 72"}
+            "note": "heads padded to 80 in the QKV projection and attention tiles; FLOPs counted at 72"}
 
 
 def official_workload(pk, reps: int = 5):

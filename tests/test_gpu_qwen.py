@@ -95,3 +95,29 @@ def test_qwen_rejects_bad_sizes(dv, encq):
     img = torch.zeros((48, 64, 3), dtype=torch.uint8, device="cuda")
     with pytest.raises(dv.DsVitError):
         encq.encode(img)
+
+
+def test_qwen_full_grid_block_repeatable(dv, wq):
+    """1024x1024 (4096 patches: 16 query blocks of 256 rows per head, 32 K/V
+    tiles): block 0 teacher-forced against the oracle, and three encodes
+    bit-identical.  The attention writes P over the scores it has read and
+    issues the next scores after the PV MMA; an ordering fault there would
+    show as run-to-run differences."""
+    cfg = WL.QWEN_MODEL
+    e = dv.QwenEncoder(dv.weights_to_device(wq), cfg, n_layers=1)
+    try:
+        img = WL.uniform_image(1024, 1024, seed=1024)
+        dimg = torch.from_numpy(img).cuda()
+        runs = []
+        for _ in range(3):
+            out, _, blocks = e.encode(dimg, deepstack=False, dump=True)
+            torch.cuda.synchronize()
+            runs.append((out.clone(), blocks.clone()))
+        for out, blocks in runs[1:]:
+            assert torch.equal(out, runs[0][0]) and torch.equal(blocks, runs[0][1])
+        bl = runs[0][1].cpu()
+        gy, gx = Q.patch_order(64, 64)
+        ref = Q.block(bits_of(bl[0]), wq["layers"][0], cfg, gy, gx)
+        assert_parity(bits_of(bl[1]), ref, what="block 0 at 4096 patches")
+    finally:
+        e.close()

@@ -2,18 +2,30 @@
 // Engineering, Part 3: Integrating Vision", comparison table: hidden 1,152,
 // 16 heads -> head_dim 72) on tcgen05.
 //
-// The QKV projection writes every head padded to 128 columns (dims 72..127
-// zero), so each Q/K/V head tile is two 128-byte-swizzled 64-column atoms and
-// the MMAs use the same descriptor forms as the head-64 kernel:
-//   S = Q K^T   (M 128, N 128, K 80: four K steps in atom 0, one in atom 1;
-//                dims 80..127 are zero and skipped)
-//   O += P V    (M 128, N 64 per atom, K 128: P from TMEM, V MN-major)
-// One CTA = (128 query rows, head); warps 0-7 softmax with two threads per
+// The QKV projection writes every head 80 columns wide (dims 72..79 zero:
+// the MMA's N and K come in steps of 16).  A Q, K or V head tile of 128 rows
+// is loaded as two TMA boxes: columns 0..63 as a 128-byte-swizzled atom
+// (16 KB) and columns 64..79 as a 32-byte-swizzled tail atom (4 KB):
+//   S_X = Q_X K_j^T  (M 128, N 128, K 80: four K steps in the atom, one in the tail)
+//   O_X += P_X V_j   (M 128, K 128; N 64 over the atom + N 16 over the tail,
+//                     P from TMEM, V MN-major)
+//
+// The schedule is the head-64 kernel's: one CTA = (256 query rows, head) as
+// two 128-row tiles A and B that share every K/V tile; warps 0-7 run the
+// softmax of tile A and warps 8-15 that of tile B with two threads per query
 // row (one per 64-key half, half-row maxima and sums exchanged through shared
-// memory), warp 8 loads Q once and streams K/V through a 2-stage TMA ring,
-// warp 9 issues the MMAs.  TMEM: S [0,128), O [128,256), P [256,320).
-// Softmax scale 1/sqrt(72); the running maximum is raised only when it grows
-// by more than 8 (log2 units), as in the head-64 kernel.  The output keeps
+// memory); the exponent math of the two tiles takes turns; warp 16 loads Q
+// once and streams K/V through a 4-stage TMA ring; warps 17 and 18 issue the
+// MMAs of tiles A and B.  The running maximum is raised only when it grows by
+// more than 8 (log2 units); the final O / l uses the same maximum, so the
+// result is the exact softmax.  Softmax scale 1/sqrt(72).
+//
+// TMEM: S_A [0,128), S_B [128,256), O_A [256,336), O_B [384,464).  An 80-wide
+// O does not fit beside separate P buffers, so P_X (bf16 pairs) is written
+// over the S_X columns that its half-row thread has already read: half h at
+// S_X + 64 h, 32 columns.  The MMA warp issues S_X(j+1) after O_X += P_X(j)
+// V_j, and tcgen05 MMAs issued by one thread run in issue order, so the next
+// scores never overwrite P before the PV MMA has read it.  The output keeps
 // the 72 real dims: out[row, head*72 + d].
 #include "internal.h"
 #include "ptx.cuh"
@@ -25,34 +37,41 @@ namespace dsvit {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kHdPad = 128;                        // padded head width in qkv
+constexpr int kHdPad = 80;                         // head width in qkv
 constexpr int kHd = 72;                            // real head dims
-constexpr int kStages = 2;
+constexpr int kHeads = 16;
+constexpr int kStages = 4;
 constexpr int kAtomBytes = kTile * 64 * 2;         // 16 KB: 128 rows x 64 bf16
-constexpr int kTileBytes = 2 * kAtomBytes;         // Q, K or V tile of one head
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTileBytes;
+constexpr int kTailBytes = kTile * 16 * 2;         // 4 KB: 128 rows x 16 bf16
+constexpr int kTileBytes = kAtomBytes + kTailBytes;
+constexpr int kOffQ = 0;                           // Q_A, Q_B
+constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
 constexpr int kOffBar = kOffV + kStages * kTileBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+static_assert(kTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 128;
-constexpr uint32_t kTmemP = 256;
-constexpr int kThreads = 320;                      // 8 softmax warps, TMA warp, MMA warp
-constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr uint32_t kTmemO = 256;                   // O_X at 256 + 128 X
+constexpr int kThreads = 608;                      // 16 softmax warps, TMA warp, 2 MMA warps
+constexpr int kWarpTma = 16;
+constexpr int kWarpMma = 17;                       // 17: tile A, 18: tile B
 constexpr float kRescaleThreshold = 8.f;
 
 enum : int {
   kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = kBarKvFull + kStages,
-  kBarSFull = kBarKvEmpty + kStages, kBarSFree, kBarPFull, kBarPvDone, kBarDrain,
-  kBarXch,                                         // [4 quadrants]
-  kBarCount = kBarXch + 4
+  kBarSFull = kBarKvEmpty + kStages,   // [2]
+  kBarPFull = kBarSFull + 2,           // [2]
+  kBarPvDone = kBarPFull + 2,          // [2]
+  kBarDrain = kBarPvDone + 2,          // [2]
+  kBarXch = kBarDrain + 2,             // [2 tiles][4 quadrants]
+  kBarTurn = kBarXch + 8,              // [2]
+  kBarCount = kBarTurn + 2
 };
 static_assert(kBarCount <= 30, "barrier area");
 
 struct QwenAttnParams {
   int n;            // rows of the image
-  int qkv_cols;     // 3 * 16 * 128
   bf16* out;        // [n, 16 * 72]
   int* status;
   float scale_log2;
@@ -87,9 +106,18 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
                  "=r"(r[7])
                : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               :
+               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                 "r"(r[7])
+               : "memory");
+}
 
-__global__ void __launch_bounds__(kThreads, 1)
-    attn_pad128_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ QwenAttnParams p) {
+// 19 warps: five share one SM sub-partition's 16K registers, so 96 a thread.
+__global__ void __maxnreg__(96)
+    attn_hd72_kernel(const __grid_constant__ CUtensorMap tm, const __grid_constant__ CUtensorMap tm_tail,
+                     const __grid_constant__ QwenAttnParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -97,11 +125,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 31);
   const uint32_t bar0 = smem_u32(bars);
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
-  const uint32_t sQ = smem_u32(smem + kOffQ);
+  auto sQ = [&](int x) { return smem_u32(smem + kOffQ + x * kTileBytes); };
   auto sK = [&](int s) { return smem_u32(smem + kOffK + s * kTileBytes); };
   auto sV = [&](int s) { return smem_u32(smem + kOffV + s * kTileBytes); };
 
-  const int q0 = static_cast<int>(blockIdx.x) * kTile;
+  const int q0 = static_cast<int>(blockIdx.x) * (2 * kTile);
   const int head = blockIdx.y;
   const int len = p.n;
   const int n_kv = (len + kTile - 1) / kTile;
@@ -110,17 +138,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(kBarKvFull + s), 1);
-      mbar_init(bar(kBarKvEmpty + s), 1);
+      mbar_init(bar(kBarKvEmpty + s), 2);      // released by both MMA warps
     }
-    mbar_init(bar(kBarSFull), 1);
-    mbar_init(bar(kBarSFree), 256);
-    mbar_init(bar(kBarPFull), 256);
-    mbar_init(bar(kBarPvDone), 1);
-    mbar_init(bar(kBarDrain), 1);
-    for (int q = 0; q < 4; ++q) mbar_init(bar(kBarXch + q), 64);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar(kBarSFull + x), 1);
+      mbar_init(bar(kBarPFull + x), 256);
+      mbar_init(bar(kBarPvDone + x), 1);
+      mbar_init(bar(kBarDrain + x), 1);
+      for (int q = 0; q < 4; ++q) mbar_init(bar(kBarXch + 4 * x + q), 64);
+      mbar_init(bar(kBarTurn + x), 256);
+    }
     fence_barrier_init();
   }
-  if (warp == kWarpTma && lane == 0) prefetch_tensormap(&tm);
+  if (warp == kWarpTma && lane == 0) {
+    prefetch_tensormap(&tm);
+    prefetch_tensormap(&tm_tail);
+  }
   if (warp == kWarpTma) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -132,44 +165,55 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_launch();
   grid_dep_wait();
 
-  __shared__ int kv_consumed;
-  __shared__ float xch[2][2][kTile];     // [parity][half][row]
+  __shared__ int kv_consumed[2];
+  __shared__ float xch[2][2][2][kTile];   // [exchange parity][tile][half][row]
   int kv_issued = 0;
   bool q_issued = false;
-  const int colq = head * kHdPad, colk = 16 * kHdPad + head * kHdPad, colv = 32 * kHdPad + head * kHdPad;
+  const int colq = head * kHdPad, colk = (kHeads + head) * kHdPad, colv = (2 * kHeads + head) * kHdPad;
 
   if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      mbar_expect_tx(bar(kBarQ), kTileBytes);
-      tma_load_2d(sQ, &tm, bar(kBarQ), colq, q0);
-      tma_load_2d(sQ + kAtomBytes, &tm, bar(kBarQ), colq + 64, q0);
+      mbar_expect_tx(bar(kBarQ), 2 * kTileBytes);
+      for (int x = 0; x < 2; ++x) {
+        tma_load_2d(sQ(x), &tm, bar(kBarQ), colq, q0 + x * kTile);
+        tma_load_2d(sQ(x) + kAtomBytes, &tm_tail, bar(kBarQ), colq + 64, q0 + x * kTile);
+      }
       q_issued = true;
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % kStages;
         if (!mbar_wait(bar(kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, p.status)) break;
         mbar_expect_tx(bar(kBarKvFull + s), 2 * kTileBytes);
         tma_load_2d(sK(s), &tm, bar(kBarKvFull + s), colk, j * kTile);
-        tma_load_2d(sK(s) + kAtomBytes, &tm, bar(kBarKvFull + s), colk + 64, j * kTile);
+        tma_load_2d(sK(s) + kAtomBytes, &tm_tail, bar(kBarKvFull + s), colk + 64, j * kTile);
         tma_load_2d(sV(s), &tm, bar(kBarKvFull + s), colv, j * kTile);
-        tma_load_2d(sV(s) + kAtomBytes, &tm, bar(kBarKvFull + s), colv + 64, j * kTile);
+        tma_load_2d(sV(s) + kAtomBytes, &tm_tail, bar(kBarKvFull + s), colv + 64, j * kTile);
         ++kv_issued;
       }
     }
-  } else if (warp == kWarpMma) {
+  } else if (warp >= kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer of tile X
+    const int x = warp - kWarpMma;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_o = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
-      const uint32_t tS = tmem, tO = tmem + kTmemO, tP = tmem + kTmemP;
+      constexpr uint32_t id_o64 = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
+      constexpr uint32_t id_o16 = idesc_bf16_f32(128, 16, false, true);
+      const uint32_t tS = tmem + x * 128, tO = tmem + kTmemO + x * 128;
       int consumed = 0;
+      // Descriptors are built once; a stage or K step only advances the start
+      // address field (byte offset >> 4).
+      const uint64_t dq = sdesc_sw128(sQ(x), 16, 1024);
+      const uint64_t dq_tail = sdesc_sw32(sQ(x) + kAtomBytes, 16, 256);
+      const uint64_t dk0 = sdesc_sw128(sK(0), 16, 1024);
+      const uint64_t dk0_tail = sdesc_sw32(sK(0) + kAtomBytes, 16, 256);
+      const uint64_t dv0 = sdesc_sw128(sV(0), kAtomBytes, 1024);
+      const uint64_t dv0_tail = sdesc_sw32(sV(0) + kAtomBytes, kTailBytes, 256);
       auto issue_s = [&](int j) {
-        const uint32_t kb = sK(j % kStages);
-        // K steps of 16 dims: 0..3 in atom 0, step 4 (dims 64..79) in atom 1.
+        const uint64_t st = static_cast<uint64_t>((j % kStages) * (kTileBytes >> 4));
 #pragma unroll
-        for (int k = 0; k < 5; ++k) {
-          const uint32_t off = (k < 4 ? k * 32 : kAtomBytes);
-          umma_bf16(tS, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), id_s, k != 0);
-        }
-        umma_commit(bar(kBarSFull));
+        for (int k = 0; k < 4; ++k) umma_bf16(tS, dq + 2 * k, dk0 + st + 2 * k, id_s, k != 0);
+        umma_bf16(tS, dq_tail, dk0_tail + st, id_s, 1u);
+        umma_commit(bar(kBarSFull + x));
       };
       bool ok = mbar_wait(bar(kBarQ), 0, p.status) && mbar_wait(bar(kBarKvFull), 0, p.status);
       if (ok) {
@@ -177,46 +221,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         issue_s(0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
-        const uint32_t par = j & 1;
+        if (!mbar_wait(bar(kBarPFull + x), j & 1, p.status)) break;
+        tc_fence_after();
+        const uint64_t st = static_cast<uint64_t>((j % kStages) * (kTileBytes >> 4));
+#pragma unroll
+        for (int k = 0; k < kTile / 16; ++k) {
+          // Keys 16k..16k+15: P half k/4, columns 8 (k % 4) of that half.
+          const uint32_t a = tS + (k >> 2) * 64 + (k & 3) * 8;
+          const uint32_t acc = (j | k) != 0;
+          umma_bf16_ts(tO, a, dv0 + st + 128 * k, id_o64, acc);         // 16 key rows x 128 B
+          umma_bf16_ts(tO + 64, a, dv0_tail + st + 32 * k, id_o16, acc);  // 16 key rows x 32 B
+        }
+        umma_commit(bar(kBarPvDone + x));
+        umma_commit(bar(kBarKvEmpty + j % kStages));
+        consumed = j + 1;
         if (j + 1 < n_kv) {
           if (!mbar_wait(bar(kBarKvFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, p.status)) break;
-          if (!mbar_wait(bar(kBarSFree), par, p.status)) break;
           tc_fence_after();
           issue_s(j + 1);
         }
-        if (!mbar_wait(bar(kBarPFull), par, p.status)) break;
-        tc_fence_after();
-        const uint32_t vb = sV(j % kStages);
-#pragma unroll
-        for (int a = 0; a < 2; ++a) {
-#pragma unroll
-          for (int k = 0; k < kTile / 16; ++k)     // 16 keys = 2048 B of an atom
-            umma_bf16_ts(tO + 64 * a, tP + k * 8, sdesc_sw128(vb + a * kAtomBytes + 2048 * k, kAtomBytes, 1024),
-                         id_o, (j | k) != 0);
-        }
-        umma_commit(bar(kBarPvDone));
-        umma_commit(bar(kBarKvEmpty + j % kStages));
-        consumed = j + 1;
       }
-      kv_consumed = consumed;
-      umma_commit(bar(kBarDrain));
-      mbar_wait(bar(kBarDrain), 0, p.status);
+      kv_consumed[x] = consumed;
+      // All MMAs of this warp complete before TMEM is released.
+      umma_commit(bar(kBarDrain + x));
+      mbar_wait(bar(kBarDrain + x), 0, p.status);
     }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-7)
+    // ------------------------------------------------------------ softmax (warps 0-15)
+    const int x = warp >> 3;                 // query tile A (0) or B (1)
     const int qd = warp & 3;                 // TMEM lane quadrant
-    const int h = warp >> 2;                 // 64-key half of the score tile
+    const int h = (warp >> 2) & 1;           // 64-key half of the score tile
     const int r = qd * 32 + lane;
     const uint32_t lane_sel = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + h * 64 + lane_sel;
-    const uint32_t tO = tmem + kTmemO + h * 64 + lane_sel;
-    const uint32_t tP = tmem + kTmemP + h * 32 + lane_sel;
-    const uint32_t xbar = bar(kBarXch + qd);
+    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;   // S half, then P half
+    const uint32_t tO = tmem + kTmemO + x * 128 + lane_sel;
+    const uint32_t xbar = bar(kBarXch + 4 * x + qd);
+    // Both threads of a row write their half's value, arrive, wait for the
+    // phase and read the other's; slot parity e alternates, so a slot is
+    // rewritten only after its reader has arrived at the next exchange.
     auto exchange = [&](float v, int e, float* other) {
-      xch[e & 1][h][r] = v;
+      xch[e & 1][x][h][r] = v;
       mbar_arrive(xbar);
       if (!mbar_wait(xbar, e & 1, p.status)) return false;
-      *other = xch[e & 1][h ^ 1][r];
+      *other = xch[e & 1][x][h ^ 1][r];
       return true;
     };
     const float c = p.scale_log2;
@@ -225,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const uint32_t par = j & 1;
-      if (!mbar_wait(bar(kBarSFull), par, p.status)) {
+      if (!mbar_wait(bar(kBarSFull + x), par, p.status)) {
         ok = false;
         break;
       }
@@ -234,8 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sr));
       tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(bar(kBarSFree));
+      // Take turns: A's step j after B's step j-1, B's step j after A's step j.
+      if (x == 1 || j > 0) {
+        if (!mbar_wait(bar(kBarTurn + (x ^ 1)), (x == 1 ? j : j - 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
+      }
       const int kv_valid = len - j * kTile - h * 64;
       if (kv_valid < 64) {
 #pragma unroll
@@ -263,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_tile = fmaxf(m_half, m_other) * c;
       float m_new = m, alpha = 1.f;
-      if (m_tile > m + kRescaleThreshold) {
+      if (m_tile > m + kRescaleThreshold) {   // always true on the first tile (m = -inf)
         m_new = m_tile;
         alpha = ex2_approx(m - m_new);
       }
@@ -279,51 +331,60 @@ __global__ void __launch_bounds__(kThreads, 1)
         acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
+      mbar_arrive(bar(kBarTurn + x));         // the other tile's turn
       const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float s0, s1;
       f2_split(s2, s0, s1);
-      l = l * alpha + (s0 + s1);
+      l = l * alpha + (s0 + s1);              // this half's share of the row sum
       if (j > 0) {
-        if (!mbar_wait(bar(kBarPvDone), par ^ 1, p.status)) {
+        // O_X is rescaled below: the previous PV MMA must be done.
+        if (!mbar_wait(bar(kBarPvDone + x), par ^ 1, p.status)) {
           ok = false;
           break;
         }
         tc_fence_after();
       }
-      tmem_st32(tP, pk);
+      // P over the S columns this thread has read (its own half).
+      tmem_st32(tS, pk);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
+        // Half h rescales O columns [40 h, 40 h + 40) (72..79 stay zero).
+        uint32_t o[32];
+        tmem_ld32(tO + h * 40, o);
+        tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          uint32_t o[32];
-          tmem_ld32(tO + q * 32, o);
+        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+        tmem_st32(tO + h * 40, o);
+        if (h == 0) {
+          uint32_t o8[8];
+          tmem_ld8(tO + 32, o8);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + q * 32, o);
+          for (int i = 0; i < 8; ++i) o8[i] = __float_as_uint(__uint_as_float(o8[i]) * alpha);
+          tmem_st8(tO + 32, o8);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(kBarPFull));
+      mbar_arrive(bar(kBarPFull + x));
       m = m_new;
     }
     float l_other = 0.f;
-    if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone), (n_kv - 1) & 1, p.status)) {
+    if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
       const float inv_l = 1.f / (l + l_other);
       // Thread h = 0 writes dims 0..39, h = 1 dims 40..71.
-      const uint32_t tOall = tmem + kTmemO + lane_sel;
       uint32_t o[40];
       if (h == 0) {
-        tmem_ld32(tOall, *reinterpret_cast<uint32_t(*)[32]>(o));
-        tmem_ld8(tOall + 32, *reinterpret_cast<uint32_t(*)[8]>(o + 32));
+        tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld8(tO + 32, *reinterpret_cast<uint32_t(*)[8]>(o + 32));
       } else {
-        tmem_ld32(tOall + 40, *reinterpret_cast<uint32_t(*)[32]>(o));
+        tmem_ld32(tO + 40, *reinterpret_cast<uint32_t(*)[32]>(o));
       }
       tmem_wait_ld();
-      const int qrow = q0 + r;
+      const int qrow = q0 + x * kTile + r;
       if (qrow < len) {
-        uint4* dst = reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * (16 * kHd) + head * kHd + h * 40);
+        uint4* dst =
+            reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * (kHeads * kHd) + head * kHd + h * 40);
         const int nq = h == 0 ? 5 : 4;
 #pragma unroll
         for (int q = 0; q < 5; ++q) {
@@ -341,8 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpTma && lane == 0 && status_failed(p.status)) {
+    // After a timeout: wait (bounded) for the loads still in flight, so no TMA
+    // write lands in shared memory after the CTA has exited.
     if (q_issued) mbar_wait(bar(kBarQ), 0, nullptr);
-    for (int j = kv_consumed; j < kv_issued; ++j)
+    const int done = kv_consumed[0] < kv_consumed[1] ? kv_consumed[0] : kv_consumed[1];
+    for (int j = done; j < kv_issued; ++j)
       if (!mbar_wait(bar(kBarKvFull + j % kStages), (j / kStages) & 1, nullptr)) break;
   }
   __syncthreads();
@@ -354,22 +418,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-int launch_attention_pad128(const CUtensorMap& tm_qkv, int n, bf16* out, int* status, cudaStream_t stream) {
+int launch_attention_hd72(const CUtensorMap& tm_qkv, const CUtensorMap& tm_qkv_tail, int n, bf16* out,
+                          int* status, cudaStream_t stream) {
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_pad128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    attr_err = cudaFuncSetAttribute(attn_hd72_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   });
   if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
   if (n <= 0) return DS_VIT_OK;
   QwenAttnParams p;
   p.n = n;
-  p.qkv_cols = 48 * kHdPad;
   p.out = out;
   p.status = status;
   p.scale_log2 = static_cast<float>(1.4426950408889634 / 8.48528137423857);   // log2(e) / sqrt(72)
-  const cudaError_t e = launch_pdl(attn_pad128_kernel, dim3((n + kTile - 1) / kTile, 16), dim3(kThreads),
-                                   kSmemBytes, stream, tm_qkv, p);
+  const cudaError_t e = launch_pdl(attn_hd72_kernel, dim3((n + 2 * kTile - 1) / (2 * kTile), kHeads),
+                                   dim3(kThreads), kSmemBytes, stream, tm_qkv, tm_qkv_tail, p);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }

@@ -751,6 +751,11 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
   return encode_tmap(map, base, rows, cols, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+bool make_tmap_bf16_tail16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows) {
+  return encode_tmap(map, base, rows, cols, 16, box_rows, CU_TENSOR_MAP_SWIZZLE_32B);
+}
+
 bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
   return encode_tmap(map, base, rows, cols, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }

@@ -42,6 +42,11 @@ enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkv
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                     uint32_t box_rows);
 
+// The same matrix with boxes [box_rows, 16 cols] and 32-byte swizzle (rows of
+// 32 B, the layout of a 16-column tail atom).
+bool make_tmap_bf16_tail16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                           uint32_t box_rows);
+
 // Store map of a row-major bf16 output [rows, cols]: 32x32 boxes, 64-byte swizzle.
 bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols);
 

@@ -266,6 +266,20 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
+// The same descriptor with 32-byte swizzle (layout type 6): a K-major operand
+// is rows of 16 bf16 (32 B) with 8-row groups SBO = 256 B apart; an MN-major
+// operand is 16 bf16 of MN per 32 B row (one row per K index), 8-row groups
+// SBO apart, 16-wide MN chunks LBO apart.  Tiles are 256-byte aligned.
+__device__ __forceinline__ uint64_t sdesc_sw32(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(6) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D: D format in
 // bits 4-5 (1 = f32), A format 7-9 (1 = bf16), B format 10-12 (1 = bf16),
 // A major bit 15 / B major bit 16 (0 = K-major, 1 = MN-major), N >> 3 in

@@ -9,7 +9,7 @@
 // Kernels here: patchify (pixels -> [N, 1536] through the prepared pixel
 // table), position-table interpolation (fp32, the same operation order as the
 // oracle), the RoPE cos/sin table and the in-place rotation of q and k, and the
-// preparation copy of W_qkv with every head padded to 128 rows.  The GEMMs,
+// preparation copy of W_qkv with every head padded to 80 rows.  The GEMMs,
 // LayerNorm and attention are the shared kernels (attention in its
 // padded-head form).  Host code: the C ABI of the tower.
 #include "internal.h"
@@ -19,12 +19,13 @@
 
 namespace dsvit {
 
-int launch_attention_pad128(const CUtensorMap& tm_qkv, int n, bf16* out, int* status, cudaStream_t stream);
+int launch_attention_hd72(const CUtensorMap& tm_qkv, const CUtensorMap& tm_qkv_tail, int n, bf16* out,
+                          int* status, cudaStream_t stream);
 
 namespace {
 
-constexpr int kD = 1152, kHeads = 16, kHd = 72, kHdPad = 128, kF = 4608, kOut = 5120;
-constexpr int kQkvPad = 3 * kHeads * kHdPad;       // 6144
+constexpr int kD = 1152, kHeads = 16, kHd = 72, kHdPad = 80, kF = 4608, kOut = 5120;
+constexpr int kQkvPad = 3 * kHeads * kHdPad;       // 3840
 constexpr int kMaxRopePos = 2048;
 constexpr int kTaps[3] = {8, 16, 24};
 
@@ -89,27 +90,40 @@ __global__ void qwen_rope_table_kernel(float* cs, int max_pos, double theta) {
   cs[pos * 36 + 18 + j] = static_cast<float>(sin(a));
 }
 
-// In place on the q and k heads of qkv [N, 6144] (head h at columns 128 h and
-// 2048 + 128 h): dims [0, 36) rotated at the patch row and [36, 72) at the
+// In place on the q and k heads of qkv [N, 3840] (head h at columns 80 h and
+// 1280 + 80 h): dims [0, 36) rotated at the patch row and [36, 72) at the
 // patch column, pairs (j, j + 18): v'[j] = v[j] c - v[j+18] s,
-// v'[j+18] = v[j+18] c + v[j] s, fp32 products rounded one at a time, stored bf16.
-__global__ void qwen_rope_kernel(bf16* __restrict__ qkv, int gw, const float* __restrict__ cs) {
-  const int r = blockIdx.x;
+// v'[j+18] = v[j+18] c + v[j] s, fp32 products rounded one at a time, stored
+// bf16.  One thread per (row, q/k, head): the head's 72 values move as nine
+// 16-byte words.
+__global__ void qwen_rope_kernel(bf16* __restrict__ qkv, int n_rows, int gw, const float* __restrict__ cs) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int r = t >> 5, qk = (t >> 4) & 1, head = t & 15;
+  if (r >= n_rows) return;
   int gy, gx;
   group_pos(r, gw, &gy, &gx);
-  // 2 (q, k) x 16 heads x 2 halves x 18 pairs
-  for (int t = threadIdx.x; t < 2 * kHeads * 2 * 18; t += blockDim.x) {
-    const int j = t % 18, half = (t / 18) & 1, head = (t / 36) % kHeads, qk = t / (36 * kHeads);
-    const int pos = half ? gx : gy;
-    const float c = cs[pos * 36 + j], s = cs[pos * 36 + 18 + j];
-    bf16* v = qkv + static_cast<size_t>(r) * kQkvPad + qk * (kHeads * kHdPad) + head * kHdPad + half * 36;
-    const float a = __bfloat162float(v[j]), b = __bfloat162float(v[j + 18]);
-    v[j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, c), __fmul_rn(b, s)));
-    v[j + 18] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, c), __fmul_rn(a, s)));
+  uint4* v4 = reinterpret_cast<uint4*>(qkv + static_cast<size_t>(r) * kQkvPad + qk * (kHeads * kHdPad) +
+                                       head * kHdPad);
+  uint4 w[9];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) w[i] = v4[i];
+  bf16* v = reinterpret_cast<bf16*>(w);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const float* c = cs + (half ? gx : gy) * 36;
+#pragma unroll
+    for (int j = 0; j < 18; ++j) {
+      const float co = __ldg(c + j), si = __ldg(c + 18 + j);
+      const float a = __bfloat162float(v[half * 36 + j]), b = __bfloat162float(v[half * 36 + 18 + j]);
+      v[half * 36 + j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si)));
+      v[half * 36 + 18 + j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si)));
+    }
   }
+#pragma unroll
+  for (int i = 0; i < 9; ++i) v4[i] = w[i];
 }
 
-// W'[(s*16 + h)*128 + d] = W[(s*16 + h)*72 + d] for d < 72, zero rows for
+// W'[(s*16 + h)*80 + d] = W[(s*16 + h)*72 + d] for d < 72, zero rows for
 // d >= 72 (s = q, k, v); bias likewise.  One block per padded row.
 __global__ void qwen_pad_qkv_kernel(const bf16* __restrict__ w, const bf16* __restrict__ b,
                                     bf16* __restrict__ wp, bf16* __restrict__ bp) {
@@ -189,7 +203,7 @@ using namespace dsvit;
 struct ds_vit_qwen_prepared {
   ds_vit_config cfg;
   ds_vit_qwen_weights w;
-  bf16* qkv_pad;      // per layer: W [6144, 1152] then b [6144]
+  bf16* qkv_pad;      // per layer: W [3840, 1152] then b [3840]
   bf16* pix_lut;      // [3, 256]
   float* rope_cs;     // [kMaxRopePos, 36]
   int* status;
@@ -322,11 +336,12 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
   bf16* ddeep = static_cast<bf16*>(deepstack);
   bf16* dblocks = static_cast<bf16*>(blocks);
 
-  CUtensorMap tA_pix, tA_y, tA_o, tA_h, tA_m, tA_u, t_qkv, tC_x, tC_qkv, tC_h, tC_u, tC_out[4];
+  CUtensorMap tA_pix, tA_y, tA_o, tA_h, tA_m, tA_u, t_qkv, t_qkv_tail, tC_x, tC_qkv, tC_h, tC_u, tC_out[4];
   if (!make_tmap_bf16(&tA_pix, h, N, 1536, 128) || !make_tmap_bf16(&tA_y, y, N, kD, 128) ||
       !make_tmap_bf16(&tA_o, o, N, kD, 128) || !make_tmap_bf16(&tA_h, h, N, kF, 128) ||
       !make_tmap_bf16(&tA_m, y, T, 4 * kD, 128) || !make_tmap_bf16(&tA_u, qkv, T, 4 * kD, 128) ||
-      !make_tmap_bf16(&t_qkv, qkv, N, kQkvPad, 128) || !make_tmap_store_bf16(&tC_x, x, N, kD) ||
+      !make_tmap_bf16(&t_qkv, qkv, N, kQkvPad, 128) || !make_tmap_bf16_tail16(&t_qkv_tail, qkv, N, kQkvPad, 128) ||
+      !make_tmap_store_bf16(&tC_x, x, N, kD) ||
       !make_tmap_store_bf16(&tC_qkv, qkv, N, kQkvPad) || !make_tmap_store_bf16(&tC_h, h, N, kF) ||
       !make_tmap_store_bf16(&tC_u, qkv, T, 4 * kD) || !make_tmap_store_bf16(&tC_out[0], dout, T, kOut))
     return DS_VIT_ECUDA;
@@ -359,9 +374,9 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
                             cfg.ln_eps, st, false, kD));
     QW_TRY(launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, kQkvPad, kD, pad_b(p, l), qkv, kEpiBias, nullptr, nullptr,
                        p->status, st));
-    qwen_rope_kernel<<<N, 256, 0, st>>>(qkv, gw, p->rope_cs);
+    qwen_rope_kernel<<<(N * 32 + 255) / 256, 256, 0, st>>>(qkv, N, gw, p->rope_cs);
     QW_CUDA(cudaGetLastError());
-    QW_TRY(launch_attention_pad128(t_qkv, N, o, p->status, st));
+    QW_TRY(launch_attention_hd72(t_qkv, t_qkv_tail, N, o, p->status, st));
     QW_TRY(launch_gemm(tA_o, p->tm_proj[l], tC_x, N, kD, kD, static_cast<const bf16*>(L.proj_b), x,
                        kEpiBiasResid, nullptr, nullptr, p->status, st));
     QW_TRY(launch_layernorm(x, static_cast<const bf16*>(L.ln2_g), static_cast<const bf16*>(L.ln2_b), y, N,

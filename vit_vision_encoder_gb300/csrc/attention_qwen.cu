@@ -3,30 +3,36 @@
 // 16 heads -> head_dim 72) on tcgen05.
 //
 // The QKV projection writes every head 80 columns wide (dims 72..79 zero:
-// the MMA's N and K come in steps of 16).  A Q, K or V head tile of 128 rows
-// is loaded as two TMA boxes: columns 0..63 as a 128-byte-swizzled atom
-// (16 KB) and columns 64..79 as a 32-byte-swizzled tail atom (4 KB):
+// the MMA's N and K come in steps of 16).  A Q or K head tile of 128 rows is
+// loaded as two TMA boxes: columns 0..63 as a 128-byte-swizzled atom (16 KB)
+// and columns 64..79 as a 32-byte-swizzled tail atom (4 KB).  A V tile is two
+// 128-byte-swizzled atoms of 64 columns: the second holds dims 64..79 and the
+// next head's first 48 columns (zero fill past the last head), of which the
+// MMA reads only the first 16:
 //   S_X = Q_X K_j^T  (M 128, N 128, K 80: four K steps in the atom, one in the tail)
-//   O_X += P_X V_j   (M 128, K 128; N 64 over the atom + N 16 over the tail,
-//                     P from TMEM, V MN-major)
+//   O_X += P_X V_j   (M 128, N 80 across the two V atoms, K 128; P from TMEM,
+//                     V MN-major)
+// (Measured on GB300: a separate N = 16 MMA for dims 64..79 cost as much as
+// a third of the kernel; one N = 80 MMA per K step does not.)
 //
 // The schedule is the head-64 kernel's: one CTA = (256 query rows, head) as
 // two 128-row tiles A and B that share every K/V tile; warps 0-7 run the
 // softmax of tile A and warps 8-15 that of tile B with two threads per query
 // row (one per 64-key half, half-row maxima and sums exchanged through shared
 // memory); the exponent math of the two tiles takes turns; warp 16 loads Q
-// once and streams K/V through a 4-stage TMA ring; warps 17 and 18 issue the
+// once and streams K/V through a 3-stage TMA ring; warps 17 and 18 issue the
 // MMAs of tiles A and B.  The running maximum is raised only when it grows by
 // more than 8 (log2 units); the final O / l uses the same maximum, so the
 // result is the exact softmax.  Softmax scale 1/sqrt(72).
 //
-// TMEM: S_A [0,128), S_B [128,256), O_A [256,336), O_B [384,464).  An 80-wide
-// O does not fit beside separate P buffers, so P_X (bf16 pairs) is written
-// over the S_X columns that its half-row thread has already read: half h at
-// S_X + 64 h, 32 columns.  The MMA warp issues S_X(j+1) after O_X += P_X(j)
-// V_j, and tcgen05 MMAs issued by one thread run in issue order, so the next
-// scores never overwrite P before the PV MMA has read it.  The output keeps
-// the 72 real dims: out[row, head*72 + d].
+// TMEM: S_A [0,128), S_B [128,256), O_A [256,336), O_B [384,464), and one P
+// buffer (bf16 pairs) that the two tiles share: keys 0..63 at [336,368), keys
+// 64..127 at [464,496).  Two 80-wide O accumulators leave no room for a P per
+// tile, but the tiles' exponent math already takes turns (A0 B0 A1 B1 ...),
+// so each tile writes P after the other tile's PV MMA that read the previous
+// P has completed; the scores stay double-buffered against the softmax as in
+// the head-64 kernel (the MMA computes S_X(j+1) once the softmax has loaded
+// S_X(j)).  The output keeps the 72 real dims: out[row, head*72 + d].
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -40,19 +46,21 @@ constexpr int kTile = 128;
 constexpr int kHdPad = 80;                         // head width in qkv
 constexpr int kHd = 72;                            // real head dims
 constexpr int kHeads = 16;
-constexpr int kStages = 4;
+constexpr int kStages = 3;
 constexpr int kAtomBytes = kTile * 64 * 2;         // 16 KB: 128 rows x 64 bf16
 constexpr int kTailBytes = kTile * 16 * 2;         // 4 KB: 128 rows x 16 bf16
-constexpr int kTileBytes = kAtomBytes + kTailBytes;
+constexpr int kTileBytes = kAtomBytes + kTailBytes;  // Q or K tile
+constexpr int kVBytes = 2 * kAtomBytes;            // V tile
 constexpr int kOffQ = 0;                           // Q_A, Q_B
 constexpr int kOffK = kOffQ + 2 * kTileBytes;
 constexpr int kOffV = kOffK + kStages * kTileBytes;
-constexpr int kOffBar = kOffV + kStages * kTileBytes;
+constexpr int kOffBar = kOffV + kStages * kVBytes;
 constexpr int kSmemBytes = kOffBar + 256 + 1024;
 static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 static_assert(kTileBytes % 1024 == 0, "tiles stay 1024-byte aligned");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256;                   // O_X at 256 + 128 X
+constexpr uint32_t kTmemP0 = 336, kTmemP1 = 464;   // P keys 0..63, 64..127
 constexpr int kThreads = 608;                      // 16 softmax warps, TMA warp, 2 MMA warps
 constexpr int kWarpTma = 16;
 constexpr int kWarpMma = 17;                       // 17: tile A, 18: tile B
@@ -61,7 +69,8 @@ constexpr float kRescaleThreshold = 8.f;
 enum : int {
   kBarQ = 0, kBarKvFull = 1, kBarKvEmpty = kBarKvFull + kStages,
   kBarSFull = kBarKvEmpty + kStages,   // [2]
-  kBarPFull = kBarSFull + 2,           // [2]
+  kBarSFree = kBarSFull + 2,           // [2]
+  kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
   kBarDrain = kBarPvDone + 2,          // [2]
   kBarXch = kBarDrain + 2,             // [2 tiles][4 quadrants]
@@ -127,7 +136,7 @@ __global__ void __maxnreg__(96)
   auto bar = [&](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
   auto sQ = [&](int x) { return smem_u32(smem + kOffQ + x * kTileBytes); };
   auto sK = [&](int s) { return smem_u32(smem + kOffK + s * kTileBytes); };
-  auto sV = [&](int s) { return smem_u32(smem + kOffV + s * kTileBytes); };
+  auto sV = [&](int s) { return smem_u32(smem + kOffV + s * kVBytes); };
 
   const int q0 = static_cast<int>(blockIdx.x) * (2 * kTile);
   const int head = blockIdx.y;
@@ -142,6 +151,7 @@ __global__ void __maxnreg__(96)
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(kBarSFull + x), 1);
+      mbar_init(bar(kBarSFree + x), 256);
       mbar_init(bar(kBarPFull + x), 256);
       mbar_init(bar(kBarPvDone + x), 1);
       mbar_init(bar(kBarDrain + x), 1);
@@ -183,11 +193,11 @@ __global__ void __maxnreg__(96)
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % kStages;
         if (!mbar_wait(bar(kBarKvEmpty + s), ((j / kStages) & 1) ^ 1, p.status)) break;
-        mbar_expect_tx(bar(kBarKvFull + s), 2 * kTileBytes);
+        mbar_expect_tx(bar(kBarKvFull + s), kTileBytes + kVBytes);
         tma_load_2d(sK(s), &tm, bar(kBarKvFull + s), colk, j * kTile);
         tma_load_2d(sK(s) + kAtomBytes, &tm_tail, bar(kBarKvFull + s), colk + 64, j * kTile);
         tma_load_2d(sV(s), &tm, bar(kBarKvFull + s), colv, j * kTile);
-        tma_load_2d(sV(s) + kAtomBytes, &tm_tail, bar(kBarKvFull + s), colv + 64, j * kTile);
+        tma_load_2d(sV(s) + kAtomBytes, &tm, bar(kBarKvFull + s), colv + 64, j * kTile);
         ++kv_issued;
       }
     }
@@ -196,8 +206,7 @@ __global__ void __maxnreg__(96)
     const int x = warp - kWarpMma;
     if (lane == 0) {
       constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);
-      constexpr uint32_t id_o64 = idesc_bf16_f32(128, 64, false, true);   // V is MN-major
-      constexpr uint32_t id_o16 = idesc_bf16_f32(128, 16, false, true);
+      constexpr uint32_t id_o = idesc_bf16_f32(128, 80, false, true);   // V is MN-major
       const uint32_t tS = tmem + x * 128, tO = tmem + kTmemO + x * 128;
       int consumed = 0;
       // Descriptors are built once; a stage or K step only advances the start
@@ -206,8 +215,8 @@ __global__ void __maxnreg__(96)
       const uint64_t dq_tail = sdesc_sw32(sQ(x) + kAtomBytes, 16, 256);
       const uint64_t dk0 = sdesc_sw128(sK(0), 16, 1024);
       const uint64_t dk0_tail = sdesc_sw32(sK(0) + kAtomBytes, 16, 256);
+      // V: 8-key groups 1024 B apart, the two 64-column atoms kAtomBytes apart.
       const uint64_t dv0 = sdesc_sw128(sV(0), kAtomBytes, 1024);
-      const uint64_t dv0_tail = sdesc_sw32(sV(0) + kAtomBytes, kTailBytes, 256);
       auto issue_s = [&](int j) {
         const uint64_t st = static_cast<uint64_t>((j % kStages) * (kTileBytes >> 4));
 #pragma unroll
@@ -221,25 +230,25 @@ __global__ void __maxnreg__(96)
         issue_s(0);
       }
       for (int j = 0; ok && j < n_kv; ++j) {
+        if (j + 1 < n_kv) {
+          // The next scores as soon as the softmax has read the current ones.
+          if (!mbar_wait(bar(kBarKvFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, p.status)) break;
+          if (!mbar_wait(bar(kBarSFree + x), j & 1, p.status)) break;
+          tc_fence_after();
+          issue_s(j + 1);
+        }
         if (!mbar_wait(bar(kBarPFull + x), j & 1, p.status)) break;
         tc_fence_after();
-        const uint64_t st = static_cast<uint64_t>((j % kStages) * (kTileBytes >> 4));
+        const uint64_t sv = static_cast<uint64_t>((j % kStages) * (kVBytes >> 4));
 #pragma unroll
         for (int k = 0; k < kTile / 16; ++k) {
-          // Keys 16k..16k+15: P half k/4, columns 8 (k % 4) of that half.
-          const uint32_t a = tS + (k >> 2) * 64 + (k & 3) * 8;
-          const uint32_t acc = (j | k) != 0;
-          umma_bf16_ts(tO, a, dv0 + st + 128 * k, id_o64, acc);         // 16 key rows x 128 B
-          umma_bf16_ts(tO + 64, a, dv0_tail + st + 32 * k, id_o16, acc);  // 16 key rows x 32 B
+          // Keys 16k..16k+15 (2048 B of each V atom): columns 8 (k % 4) of P half k / 4.
+          const uint32_t a = tmem + (k < 4 ? kTmemP0 : kTmemP1) + (k & 3) * 8;
+          umma_bf16_ts(tO, a, dv0 + sv + 128 * k, id_o, (j | k) != 0);
         }
         umma_commit(bar(kBarPvDone + x));
         umma_commit(bar(kBarKvEmpty + j % kStages));
         consumed = j + 1;
-        if (j + 1 < n_kv) {
-          if (!mbar_wait(bar(kBarKvFull + (j + 1) % kStages), ((j + 1) / kStages) & 1, p.status)) break;
-          tc_fence_after();
-          issue_s(j + 1);
-        }
       }
       kv_consumed[x] = consumed;
       // All MMAs of this warp complete before TMEM is released.
@@ -253,8 +262,9 @@ __global__ void __maxnreg__(96)
     const int h = (warp >> 2) & 1;           // 64-key half of the score tile
     const int r = qd * 32 + lane;
     const uint32_t lane_sel = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;   // S half, then P half
+    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;
     const uint32_t tO = tmem + kTmemO + x * 128 + lane_sel;
+    const uint32_t tP = tmem + (h ? kTmemP1 : kTmemP0) + lane_sel;
     const uint32_t xbar = bar(kBarXch + 4 * x + qd);
     // Both threads of a row write their half's value, arrive, wait for the
     // phase and read the other's; slot parity e alternates, so a slot is
@@ -281,6 +291,8 @@ __global__ void __maxnreg__(96)
       tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(sr));
       tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
       tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
       // Take turns: A's step j after B's step j-1, B's step j after A's step j.
       if (x == 1 || j > 0) {
         if (!mbar_wait(bar(kBarTurn + (x ^ 1)), (x == 1 ? j : j - 1) & 1, p.status)) {
@@ -336,16 +348,19 @@ __global__ void __maxnreg__(96)
       float s0, s1;
       f2_split(s2, s0, s1);
       l = l * alpha + (s0 + s1);              // this half's share of the row sum
-      if (j > 0) {
-        // O_X is rescaled below: the previous PV MMA must be done.
-        if (!mbar_wait(bar(kBarPvDone + x), par ^ 1, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+      // O_X is rescaled below: its previous PV MMA must be done.  P is
+      // rewritten: the PV MMA that read the last P (B's step j-1 before A's
+      // step j, A's step j before B's step j) must be done.
+      if (j > 0 && !mbar_wait(bar(kBarPvDone + x), par ^ 1, p.status)) {
+        ok = false;
+        break;
       }
-      // P over the S columns this thread has read (its own half).
-      tmem_st32(tS, pk);
+      if ((x == 1 || j > 0) && !mbar_wait(bar(kBarPvDone + (x ^ 1)), (x == 1 ? j : j - 1) & 1, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32(tP, pk);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         // Half h rescales O columns [40 h, 40 h + 40) (72..79 stay zero).
         uint32_t o[32];
@@ -372,29 +387,31 @@ __global__ void __maxnreg__(96)
     if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
       const float inv_l = 1.f / (l + l_other);
-      // Thread h = 0 writes dims 0..39, h = 1 dims 40..71.
-      uint32_t o[40];
-      if (h == 0) {
-        tmem_ld32(tO, *reinterpret_cast<uint32_t(*)[32]>(o));
-        tmem_ld8(tO + 32, *reinterpret_cast<uint32_t(*)[8]>(o + 32));
-      } else {
-        tmem_ld32(tO + 40, *reinterpret_cast<uint32_t(*)[32]>(o));
-      }
-      tmem_wait_ld();
+      // Thread h = 0 writes dims 0..39, h = 1 dims 40..71: 32 columns, then
+      // (h = 0) the 8 columns 32..39.
       const int qrow = q0 + x * kTile + r;
-      if (qrow < len) {
-        uint4* dst =
-            reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * (kHeads * kHd) + head * kHd + h * 40);
-        const int nq = h == 0 ? 5 : 4;
+      uint4* dst =
+          reinterpret_cast<uint4*>(p.out + static_cast<size_t>(qrow) * (kHeads * kHd) + head * kHd + h * 40);
+      auto put8 = [&](uint4* d, const uint32_t* o) {
+        *d = make_uint4(pack_bf16x2(__uint_as_float(o[0]) * inv_l, __uint_as_float(o[1]) * inv_l),
+                        pack_bf16x2(__uint_as_float(o[2]) * inv_l, __uint_as_float(o[3]) * inv_l),
+                        pack_bf16x2(__uint_as_float(o[4]) * inv_l, __uint_as_float(o[5]) * inv_l),
+                        pack_bf16x2(__uint_as_float(o[6]) * inv_l, __uint_as_float(o[7]) * inv_l));
+      };
+      {
+        uint32_t o[32];
+        tmem_ld32(tO + h * 40, o);
+        tmem_wait_ld();
+        if (qrow < len) {
 #pragma unroll
-        for (int q = 0; q < 5; ++q) {
-          if (q < nq)
-            dst[q] = make_uint4(
-                pack_bf16x2(__uint_as_float(o[q * 8 + 0]) * inv_l, __uint_as_float(o[q * 8 + 1]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[q * 8 + 2]) * inv_l, __uint_as_float(o[q * 8 + 3]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[q * 8 + 4]) * inv_l, __uint_as_float(o[q * 8 + 5]) * inv_l),
-                pack_bf16x2(__uint_as_float(o[q * 8 + 6]) * inv_l, __uint_as_float(o[q * 8 + 7]) * inv_l));
+          for (int q = 0; q < 4; ++q) put8(dst + q, o + 8 * q);
         }
+      }
+      if (h == 0) {
+        uint32_t o[8];
+        tmem_ld8(tO + 32, o);
+        tmem_wait_ld();
+        if (qrow < len) put8(dst + 4, o);
       }
     }
   }

@@ -94,33 +94,31 @@ __global__ void qwen_rope_table_kernel(float* cs, int max_pos, double theta) {
 // 1280 + 80 h): dims [0, 36) rotated at the patch row and [36, 72) at the
 // patch column, pairs (j, j + 18): v'[j] = v[j] c - v[j+18] s,
 // v'[j+18] = v[j+18] c + v[j] s, fp32 products rounded one at a time, stored
-// bf16.  One thread per (row, q/k, head): the head's 72 values move as nine
-// 16-byte words.
-__global__ void qwen_rope_kernel(bf16* __restrict__ qkv, int n_rows, int gw, const float* __restrict__ cs) {
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  const int r = t >> 5, qk = (t >> 4) & 1, head = t & 15;
-  if (r >= n_rows) return;
+// bf16.  One block per row: the row's 2560 q and k values are staged in
+// shared memory with 16-byte accesses, then rotated, 9 pairs a thread.
+constexpr int kRopeThreads = 128;
+__global__ void __launch_bounds__(kRopeThreads) qwen_rope_kernel(bf16* __restrict__ qkv, int gw,
+                                                                 const float* __restrict__ cs) {
+  constexpr int kVecs = 2 * kHeads * kHdPad / 8;   // 320 uint4
+  __shared__ uint4 buf[kVecs];
+  const int r = blockIdx.x;
   int gy, gx;
   group_pos(r, gw, &gy, &gx);
-  uint4* v4 = reinterpret_cast<uint4*>(qkv + static_cast<size_t>(r) * kQkvPad + qk * (kHeads * kHdPad) +
-                                       head * kHdPad);
-  uint4 w[9];
-#pragma unroll
-  for (int i = 0; i < 9; ++i) w[i] = v4[i];
-  bf16* v = reinterpret_cast<bf16*>(w);
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  uint4* row = reinterpret_cast<uint4*>(qkv + static_cast<size_t>(r) * kQkvPad);
+  for (int i = threadIdx.x; i < kVecs; i += kRopeThreads) buf[i] = row[i];
+  __syncthreads();
+  bf16* v = reinterpret_cast<bf16*>(buf);
+  for (int i = threadIdx.x; i < 2 * kHeads * 2 * 18; i += kRopeThreads) {
+    const int j = i % 18, half = (i / 18) & 1, hq = i / 36;   // hq = (q or k) * 16 + head
+    bf16* e = v + hq * kHdPad + half * 36 + j;
     const float* c = cs + (half ? gx : gy) * 36;
-#pragma unroll
-    for (int j = 0; j < 18; ++j) {
-      const float co = __ldg(c + j), si = __ldg(c + 18 + j);
-      const float a = __bfloat162float(v[half * 36 + j]), b = __bfloat162float(v[half * 36 + 18 + j]);
-      v[half * 36 + j] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si)));
-      v[half * 36 + 18 + j] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si)));
-    }
+    const float co = __ldg(c + j), si = __ldg(c + 18 + j);
+    const float a = __bfloat162float(e[0]), b = __bfloat162float(e[18]);
+    e[0] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si)));
+    e[18] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si)));
   }
-#pragma unroll
-  for (int i = 0; i < 9; ++i) v4[i] = w[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < kVecs; i += kRopeThreads) row[i] = buf[i];
 }
 
 // W'[(s*16 + h)*80 + d] = W[(s*16 + h)*72 + d] for d < 72, zero rows for
@@ -374,7 +372,7 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
                             cfg.ln_eps, st, false, kD));
     QW_TRY(launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, kQkvPad, kD, pad_b(p, l), qkv, kEpiBias, nullptr, nullptr,
                        p->status, st));
-    qwen_rope_kernel<<<(N * 32 + 255) / 256, 256, 0, st>>>(qkv, N, gw, p->rope_cs);
+    qwen_rope_kernel<<<N, kRopeThreads, 0, st>>>(qkv, gw, p->rope_cs);
     QW_CUDA(cudaGetLastError());
     QW_TRY(launch_attention_hd72(t_qkv, t_qkv_tail, N, o, p->status, st));
     QW_TRY(launch_gemm(tA_o, p->tm_proj[l], tC_x, N, kD, kD, static_cast<const bf16*>(L.proj_b), x,

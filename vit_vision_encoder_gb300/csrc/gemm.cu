@@ -631,6 +631,31 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
               v[q * 8 + 2 * e + 1] = __fadd_rn(bf16hi(xw[e]), v[q * 8 + 2 * e + 1]);
             }
           }
+        } else if constexpr (EPI == kEpiQkvRope72) {
+          // q and k: r(rot(r(t))).  Each 16-column group holds 8 rotation
+          // pairs (i, i + 8); rope_cs[row][slot] = (cos, sin) of pair slot
+          // 8 g + i of group g = (column mod 80) / 16.
+          if (n0 < kQwenQkCols && valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+            const float4* rt = reinterpret_cast<const float4*>(p.rope_cs + static_cast<size_t>(row) * 80);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int g = ((n0 + 16 * t) % 80) / 16;
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                const float4 cs = __ldg(rt + 4 * g + q);    // slots 2q, 2q + 1 of the group
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int i = 16 * t + 2 * q + e;
+                  const float co = e ? cs.z : cs.x, si = e ? cs.w : cs.y;
+                  const float a = v[i], b = v[i + 8];
+                  v[i] = __fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si));
+                  v[i + 8] = __fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si));
+                }
+              }
+            }
+          }
         } else if constexpr (EPI == kEpiQkvRope) {
           if (rotate) {
 #pragma unroll
@@ -787,6 +812,7 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
       case kEpiBiasGelu: return launch_gemm_t<128, kEpiBiasGelu>(tmA, tmB, tmC, p, stream);
       case kEpiBiasResid: return launch_gemm_t<128, kEpiBiasResid>(tmA, tmB, tmC, p, stream);
       case kEpiQkvRope: return launch_gemm_t<128, kEpiQkvRope>(tmA, tmB, tmC, p, stream);
+      case kEpiQkvRope72: return launch_gemm_t<128, kEpiQkvRope72>(tmA, tmB, tmC, p, stream);
       default: return DS_VIT_EINVAL;
     }
   }
@@ -796,6 +822,7 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
     case kEpiBiasGelu: return launch_gemm_t<256, kEpiBiasGelu>(tmA, tmB, tmC, p, stream);
     case kEpiBiasResid: return launch_gemm_t<256, kEpiBiasResid>(tmA, tmB, tmC, p, stream);
     case kEpiQkvRope: return launch_gemm_t<256, kEpiQkvRope>(tmA, tmB, tmC, p, stream);
+    case kEpiQkvRope72: return launch_gemm_t<256, kEpiQkvRope72>(tmA, tmB, tmC, p, stream);
     default: return DS_VIT_EINVAL;
   }
 }

@@ -34,7 +34,12 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Epilogue kinds of the tcgen05 GEMM (same values as DS_VIT_EPI_*).
-enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3, kEpiSwiglu = 4 };
+enum Epilogue : int { kEpiBias = 0, kEpiBiasGelu = 1, kEpiBiasResid = 2, kEpiQkvRope = 3, kEpiSwiglu = 4,
+                      // Internal: the Qwen-style tower's QKV (80-wide heads, rotation pairs 8
+                      // columns apart in 16-column groups, per-row cos/sin table in rope_cs).
+                      kEpiQkvRope72 = 5 };
+// q and k columns of that QKV output (2 x 16 heads x 80); V follows.
+constexpr int kQwenQkCols = 2560;
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point.
 // Row-major bf16 matrix [rows, cols], box [box_rows, 64 cols], 128-byte swizzle,

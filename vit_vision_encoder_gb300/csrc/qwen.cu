@@ -8,10 +8,11 @@
 //
 // Kernels here: patchify (pixels -> [N, 1536] through the prepared pixel
 // table), position-table interpolation (fp32, the same operation order as the
-// oracle), the RoPE cos/sin table and the in-place rotation of q and k, and the
-// preparation copy of W_qkv with every head padded to 80 rows.  The GEMMs,
-// LayerNorm and attention are the shared kernels (attention in its
-// padded-head form).  Host code: the C ABI of the tower.
+// oracle), the RoPE cos/sin tables (per position, then per patch row and pair
+// slot), and the preparation copy of W_qkv with every head padded to 80 rows
+// (q and k columns reordered so that the QKV GEMM's epilogue applies the
+// rotation).  The GEMMs, LayerNorm and attention are the shared kernels
+// (attention in its head-72 form).  Host code: the C ABI of the tower.
 #include "internal.h"
 
 #include <algorithm>
@@ -90,45 +91,60 @@ __global__ void qwen_rope_table_kernel(float* cs, int max_pos, double theta) {
   cs[pos * 36 + 18 + j] = static_cast<float>(sin(a));
 }
 
-// In place on the q and k heads of qkv [N, 3840] (head h at columns 80 h and
-// 1280 + 80 h): dims [0, 36) rotated at the patch row and [36, 72) at the
-// patch column, pairs (j, j + 18): v'[j] = v[j] c - v[j+18] s,
-// v'[j+18] = v[j+18] c + v[j] s, fp32 products rounded one at a time, stored
-// bf16.  One block per row: the row's 2560 q and k values are staged in
-// shared memory with 16-byte accesses, then rotated, 9 pairs a thread.
-constexpr int kRopeThreads = 128;
-__global__ void __launch_bounds__(kRopeThreads) qwen_rope_kernel(bf16* __restrict__ qkv, int gw,
-                                                                 const float* __restrict__ cs) {
-  constexpr int kVecs = 2 * kHeads * kHdPad / 8;   // 320 uint4
-  __shared__ uint4 buf[kVecs];
-  const int r = blockIdx.x;
+// Column order inside an 80-wide q or k head: the 36 rotation pairs (dims
+// (36 half + j, 36 half + 18 + j), half 0 at the patch row, half 1 at the
+// patch column) fill pair slots s = 0..35 of five 16-column groups, slot
+// s = 8 g + i holding its two dims at columns 16 g + i and 16 g + 8 + i; slots
+// 36..39 are zero.  q and k share the order, so Q K^T is unchanged; the QKV
+// GEMM epilogue rotates each pair inside one 32-column chunk.  V keeps the
+// natural order.  Returns the source dim of column c, or -1 for a zero column.
+__host__ __device__ constexpr int qk_source_dim(int c) {
+  const int g = c / 16, w = c % 16, slot = 8 * g + (w % 8);
+  return slot >= 36 ? -1 : 36 * (slot / 18) + slot % 18 + 18 * (w / 8);
+}
+// Every dim 0..71 appears exactly once among the 80 columns.
+constexpr bool qk_order_is_permutation() {
+  int seen[kHd] = {};
+  for (int c = 0; c < kHdPad; ++c) {
+    const int d = qk_source_dim(c);
+    if (d >= kHd) return false;
+    if (d >= 0) ++seen[d];
+  }
+  for (int d = 0; d < kHd; ++d)
+    if (seen[d] != 1) return false;
+  return true;
+}
+static_assert(qk_order_is_permutation(), "q/k column order");
+static_assert(kQwenQkCols == 2 * kHeads * kHdPad, "q and k columns of the QKV output");
+
+// rt[r][slot] = (cos, sin) of pair slot `slot` at patch row r (merge-group
+// order): slots 0..17 at the patch row gy with frequency j = slot, 18..35 at
+// the column gx with j = slot - 18, 36..39 (1, 0).  Built once per encode
+// from the [pos][cos 0..17, sin 0..17] table.
+__global__ void qwen_rope_rows_kernel(float2* __restrict__ rt, int n_rows, int gw, const float* __restrict__ cs) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * 40) return;
+  const int r = i / 40, slot = i % 40;
   int gy, gx;
   group_pos(r, gw, &gy, &gx);
-  uint4* row = reinterpret_cast<uint4*>(qkv + static_cast<size_t>(r) * kQkvPad);
-  for (int i = threadIdx.x; i < kVecs; i += kRopeThreads) buf[i] = row[i];
-  __syncthreads();
-  bf16* v = reinterpret_cast<bf16*>(buf);
-  for (int i = threadIdx.x; i < 2 * kHeads * 2 * 18; i += kRopeThreads) {
-    const int j = i % 18, half = (i / 18) & 1, hq = i / 36;   // hq = (q or k) * 16 + head
-    bf16* e = v + hq * kHdPad + half * 36 + j;
-    const float* c = cs + (half ? gx : gy) * 36;
-    const float co = __ldg(c + j), si = __ldg(c + 18 + j);
-    const float a = __bfloat162float(e[0]), b = __bfloat162float(e[18]);
-    e[0] = __float2bfloat16_rn(__fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si)));
-    e[18] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si)));
+  float2 v = make_float2(1.f, 0.f);
+  if (slot < 36) {
+    const int pos = slot < 18 ? gy : gx, j = slot % 18;
+    v = make_float2(cs[pos * 36 + j], cs[pos * 36 + 18 + j]);
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < kVecs; i += kRopeThreads) row[i] = buf[i];
+  rt[i] = v;
 }
 
-// W'[(s*16 + h)*80 + d] = W[(s*16 + h)*72 + d] for d < 72, zero rows for
-// d >= 72 (s = q, k, v); bias likewise.  One block per padded row.
+// W'[(s*16 + h)*80 + c] = W[(s*16 + h)*72 + d(c)] with d(c) = qk_source_dim(c)
+// for q and k (s = 0, 1) and d(c) = c for v, zero rows where d(c) is -1 or
+// >= 72; bias likewise.  One block per padded row.
 __global__ void qwen_pad_qkv_kernel(const bf16* __restrict__ w, const bf16* __restrict__ b,
                                     bf16* __restrict__ wp, bf16* __restrict__ bp) {
   const int r = blockIdx.x;
-  const int head = r / kHdPad, d = r % kHdPad;
-  const bool real = d < kHd;
-  const size_t src = static_cast<size_t>(head) * kHd + d;
+  const int head = r / kHdPad, c = r % kHdPad;
+  const int d = head < 2 * kHeads ? qk_source_dim(c) : c;
+  const bool real = d >= 0 && d < kHd;
+  const size_t src = static_cast<size_t>(head) * kHd + (real ? d : 0);
   for (int k = threadIdx.x; k < kD; k += blockDim.x)
     wp[static_cast<size_t>(r) * kD + k] = real ? w[src * kD + k] : __float2bfloat16_rn(0.f);
   if (threadIdx.x == 0) bp[r] = real ? b[src] : __float2bfloat16_rn(0.f);
@@ -173,7 +189,7 @@ int check_qwen_weights(const ds_vit_qwen_weights* w, int n_layers) {
 
 struct QwenPlan {
   int64_t N, T;
-  size_t off_x, off_y, off_o, off_qkv, off_h, total;
+  size_t off_x, off_y, off_o, off_qkv, off_h, off_rope, total;
 };
 
 int qwen_plan(int32_t H, int32_t W, QwenPlan* pl) {
@@ -188,6 +204,7 @@ int qwen_plan(int32_t H, int32_t W, QwenPlan* pl) {
   pl->off_o = o;   o += align_up(static_cast<size_t>(N) * kD * 2);
   pl->off_qkv = o; o += align_up(static_cast<size_t>(N) * kQkvPad * 2);   // also the merger hidden
   pl->off_h = o;   o += align_up(static_cast<size_t>(N) * kF * 2);        // also the patch matrix
+  pl->off_rope = o; o += align_up(static_cast<size_t>(N) * 40 * 8);     // per-row cos/sin of the pair slots
   pl->total = o;
   return DS_VIT_OK;
 }
@@ -330,6 +347,7 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
   bf16* o = reinterpret_cast<bf16*>(wsb + pl.off_o);
   bf16* qkv = reinterpret_cast<bf16*>(wsb + pl.off_qkv);
   bf16* h = reinterpret_cast<bf16*>(wsb + pl.off_h);
+  float2* rope_rows = reinterpret_cast<float2*>(wsb + pl.off_rope);
   bf16* dout = static_cast<bf16*>(out);
   bf16* ddeep = static_cast<bf16*>(deepstack);
   bf16* dblocks = static_cast<bf16*>(blocks);
@@ -361,6 +379,7 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
   };
 
   qwen_patch_kernel<<<N, 256, 0, st>>>(pixels, W, gw, p->pix_lut, h);
+  qwen_rope_rows_kernel<<<(N * 40 + 255) / 256, 256, 0, st>>>(rope_rows, N, gw, p->rope_cs);
   qwen_pos_kernel<<<N, 256, 0, st>>>(static_cast<const bf16*>(w.pos_table), gh, gw, x);
   QW_CUDA(cudaGetLastError());
   QW_TRY(launch_gemm(tA_pix, p->tm_patch, tC_x, N, kD, 1536, static_cast<const bf16*>(w.patch_b), x,
@@ -370,10 +389,8 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
     const ds_vit_layer_weights& L = w.layers[l];
     QW_TRY(launch_layernorm(x, static_cast<const bf16*>(L.ln1_g), static_cast<const bf16*>(L.ln1_b), y, N,
                             cfg.ln_eps, st, false, kD));
-    QW_TRY(launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, kQkvPad, kD, pad_b(p, l), qkv, kEpiBias, nullptr, nullptr,
-                       p->status, st));
-    qwen_rope_kernel<<<N, kRopeThreads, 0, st>>>(qkv, gw, p->rope_cs);
-    QW_CUDA(cudaGetLastError());
+    QW_TRY(launch_gemm(tA_y, p->tm_qkv[l], tC_qkv, N, kQkvPad, kD, pad_b(p, l), qkv, kEpiQkvRope72, nullptr,
+                       reinterpret_cast<const float*>(rope_rows), p->status, st));
     QW_TRY(launch_attention_hd72(t_qkv, t_qkv_tail, N, o, p->status, st));
     QW_TRY(launch_gemm(tA_o, p->tm_proj[l], tC_x, N, kD, kD, static_cast<const bf16*>(L.proj_b), x,
                        kEpiBiasResid, nullptr, nullptr, p->status, st));

@@ -121,3 +121,28 @@ def test_qwen_full_grid_block_repeatable(dv, wq):
         assert_parity(bits_of(bl[1]), ref, what="block 0 at 4096 patches")
     finally:
         e.close()
+
+
+def test_qwen_peaked_attention(dv, wq):
+    """q and k projection rows scaled x8 (logits of standard deviation ~10 in
+    log2 units): the running maximum rises by more than 8 inside a row, so the
+    head-72 kernel rescales O and the row sum mid-row.  512x512 image (1024
+    patches, 8 K/V tiles per row); block 0 teacher-forced."""
+    cfg = WL.QWEN_MODEL
+    L0 = dict(wq["layers"][0])
+    w = O.bits_to_f32(L0["qkv_w"]).copy()
+    w[:2 * 1152] *= 8.0
+    L0["qkv_w"] = WL.to_bf16_bits(w)
+    wp = dict(wq)
+    wp["layers"] = [L0]
+    e = dv.QwenEncoder(dv.weights_to_device(wp), cfg, n_layers=1)
+    try:
+        img = WL.uniform_image(512, 512, seed=512)
+        _, _, blocks = e.encode(torch.from_numpy(img).cuda(), deepstack=False, dump=True)
+        torch.cuda.synchronize()
+        bl = blocks.cpu()
+        gy, gx = Q.patch_order(32, 32)
+        ref = Q.block(bits_of(bl[0]), L0, cfg, gy, gx)
+        assert_parity(bits_of(bl[1]), ref, what="peaked block 0")
+    finally:
+        e.close()

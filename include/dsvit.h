@@ -375,8 +375,9 @@ typedef struct ds_vit_qwen_weights {
 
 typedef struct ds_vit_qwen_prepared ds_vit_qwen_prepared;
 
-/* Device copies (W_qkv with every head padded to 128 rows, the pixel table,
- * the RoPE table) and TMA descriptors.  Synchronises `stream`. */
+/* Device copies (W_qkv with every head padded to 80 rows, the q and k rows of
+ * each head reordered so that rotation pairs share a 16-row group; the pixel
+ * table; the RoPE table) and TMA descriptors.  Synchronises `stream`. */
 int ds_vit_qwen_prepare(const ds_vit_config* cfg, const ds_vit_qwen_weights* w,
                         ds_vit_qwen_prepared** out, void* stream);
 int ds_vit_qwen_release(ds_vit_qwen_prepared* p);

@@ -52,6 +52,9 @@ GEMM_CASES = [
     (1, 64, 256, "bias"), (77, 640, 1024, "bias"), (300, 1024, 1024, "bias"),
     (1000, 1024, 4096, "gelu"), (513, 4096, 1024, "resid"), (169, 9216, 5120, "gelu"),
     (2000, 1024, 1024, "resid"),
+    # N % 256 == 128 with many rows (N = 1152 is the Qwen-style tower's hidden
+    # width; 128-wide tiles, ragged M in the second case).
+    (4096, 1152, 1152, "resid"), (3000, 1152, 1152, "bias"), (2500, 640, 1408, "gelu"),
 ]
 
 

@@ -288,8 +288,10 @@ __global__ void __maxnreg__(96)
       }
       tc_fence_after();
       uint32_t sr[64];
-      tmem_ld64(tS, sr);   // one load: fewer instructions and registers than two of 32
+      // One load of the 64 scores that also reduces them to their maximum.
+      float m_half = tmem_ld64_max(tS, sr);
       tmem_wait_ld();
+      m_half = tmem_after_wait(m_half);
       tc_fence_before();
       mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
       // Take turns: A's step j after B's step j-1, B's step j after A's step j.
@@ -301,24 +303,15 @@ __global__ void __maxnreg__(96)
       }
       const int kv_valid = len - j * kTile - h * 64;
       if (kv_valid < 64) {
+        // Keys past the image: masked, and the maximum taken over the rest.
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 64; ++i)
+        for (int i = 0; i < 64; ++i) {
           if (i >= kv_valid) sr[i] = __float_as_uint(-INFINITY);
+          mx[i & 3] = fmaxf(mx[i & 3], __uint_as_float(sr[i]));
+        }
+        m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      float mx[4];
-#pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const uint32_t* v = sr + 16 * g;
-        float a = max3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
-        a = max3(a, __uint_as_float(v[3]), __uint_as_float(v[4]));
-        a = max3(a, __uint_as_float(v[5]), __uint_as_float(v[6]));
-        a = max3(a, __uint_as_float(v[7]), __uint_as_float(v[8]));
-        a = max3(a, __uint_as_float(v[9]), __uint_as_float(v[10]));
-        a = max3(a, __uint_as_float(v[11]), __uint_as_float(v[12]));
-        a = max3(a, __uint_as_float(v[13]), __uint_as_float(v[14]));
-        mx[g] = fmaxf(a, __uint_as_float(v[15]));
-      }
-      const float m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       float m_other;
       if (!exchange(m_half, j, &m_other)) {
         ok = false;

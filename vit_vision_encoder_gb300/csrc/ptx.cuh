@@ -76,6 +76,32 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* st
   return true;
 }
 
+// As mbar_wait for a wait expected to last, with each try suspending the
+// thread for up to `hint_ns` (it resumes when the phase completes), so a
+// waiting warp polls less often.
+__device__ __forceinline__ bool mbar_wait_sleepy(uint32_t bar, uint32_t parity, uint32_t hint_ns, int* status) {
+  auto try_once = [&]() {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+  };
+  if (try_once()) return true;
+  const unsigned long long t0 = global_timer();
+  while (!try_once()) {
+    if (global_timer() - t0 > kWaitLimitNs) {
+      report_error(status, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 // ------------------------------------------------------------------ TMA
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,

@@ -417,6 +417,18 @@ int ds_vit_qwen_layout(int32_t h, int32_t w, int32_t seq_start, int32_t* pos, in
  * or DS_VIT_ETIMEOUT if a kernel's bounded wait gave up since the last read. */
 int ds_vit_device_status(const ds_vit_prepared* p, void* stream);
 
+/*
+ * ds_vit_selftest_wait_timeout: the failure path of every bounded wait, on the
+ * device, without a fault.  One thread waits on a shared-memory mbarrier that
+ * nothing completes; after limit_us microseconds of %globaltimer it gives up,
+ * sets *status (device int32, caller-owned; not cleared first) to
+ * DS_VIT_ETIMEOUT as a timed-out kernel does, stores the time it waited in
+ * *elapsed_ns (device uint64) and returns.  The context stays usable.
+ * 1 <= limit_us <= 1000000, non-NULL pointers, else DS_VIT_EINVAL (nothing
+ * launched).  Asynchronous on `stream`.
+ */
+int ds_vit_selftest_wait_timeout(int32_t* status, uint64_t* elapsed_ns, uint32_t limit_us, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Single-kernel entry points (the steps of the encode, for step-level parity
  * checks and profiling).  `status` is a caller-owned device int32 that kernels

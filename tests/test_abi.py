@@ -85,6 +85,11 @@ def test_null_arguments_rejected_before_cuda(dv):
     assert L.ds_vit_encode(None, None, 84, 84, None, None, 0, None) == dv.EINVAL
     assert L.ds_vit_release(None) == dv.OK
     assert L.ds_vit_device_status(None, None) == dv.EINVAL
+    fake = C.c_void_p(16)   # never dereferenced: the checks reject before any launch
+    assert L.ds_vit_selftest_wait_timeout(None, fake, 1000, None) == dv.EINVAL
+    assert L.ds_vit_selftest_wait_timeout(fake, None, 1000, None) == dv.EINVAL
+    assert L.ds_vit_selftest_wait_timeout(fake, fake, 0, None) == dv.EINVAL
+    assert L.ds_vit_selftest_wait_timeout(fake, fake, 1000001, None) == dv.EINVAL
     assert L.ds_vit_op_attention(None, None, 1, None, None, None) == dv.EINVAL
     assert L.ds_vit_op_linear(None, 1, 64, None, 256, None, None, 0, None, None, None, None) == dv.EINVAL
 

@@ -96,6 +96,7 @@ SIGNATURES = {
     "ds_vit_overlay_chunk": (C.c_int, [_VP, _I64, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP,
                                        _VP, _VP]),
     "ds_vit_device_status": (C.c_int, [_VP, _VP]),
+    "ds_vit_selftest_wait_timeout": (C.c_int, [_VP, _VP, C.c_uint32, _VP]),
     "ds_vit_set_kernel_timer": (C.c_int, [_VP, C.POINTER(_VP), _P_I32, _I32, _P_I32]),
     "ds_vit_op_layernorm": (C.c_int, [_VP, _VP, _VP, _VP, _I64, _F, _VP]),
     "ds_vit_op_rmsnorm": (C.c_int, [_VP, _VP, _VP, _I64, _F, _VP]),
@@ -441,6 +442,18 @@ def overlay_chunk(chunk, chunk_begin, spans, embeds, sentinel, row_type=None):
 
 
 # ---------------------------------------------------------------- single kernels
+
+def selftest_wait_timeout(limit_us: int):
+    """Run the device bounded-wait self-test (ds_vit_selftest_wait_timeout);
+    returns (status code written by the kernel, nanoseconds it waited)."""
+    torch = _torch()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    el = torch.zeros(1, dtype=torch.int64, device="cuda")
+    check(lib.ds_vit_selftest_wait_timeout(_ptr(st), _ptr(el), int(limit_us), _stream()),
+          "ds_vit_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(st.item()), int(el.item())
+
 
 def op_layernorm(x, g, b, eps=1e-6, out=None):
     torch = _torch()

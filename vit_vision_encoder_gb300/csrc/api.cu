@@ -566,6 +566,12 @@ int ds_vit_device_status(const ds_vit_prepared* p, void* stream) {
   return v == 0 ? DS_VIT_OK : v;
 }
 
+int ds_vit_selftest_wait_timeout(int32_t* status, uint64_t* elapsed_ns, uint32_t limit_us, void* stream) {
+  if (!status || !elapsed_ns || limit_us < 1 || limit_us > 1000000) return DS_VIT_EINVAL;
+  return launch_selftest_wait(reinterpret_cast<int*>(status), reinterpret_cast<unsigned long long*>(elapsed_ns),
+                              static_cast<unsigned long long>(limit_us) * 1000ull, static_cast<cudaStream_t>(stream));
+}
+
 int ds_vit_op_layernorm(const void* x, const void* g, const void* b, void* y, int64_t M, float eps,
                         void* stream) {
   if (!x || !g || !b || !y || M < 0 || !(eps > 0.f)) return DS_VIT_EINVAL;

@@ -114,6 +114,11 @@ struct PixelNorm {
 // lut[c * 256 + v] = bf16((v/255 - mean_c)/std_c), fp32 arithmetic (3 x 256 entries).
 int launch_pixel_lut(const PixelNorm& norm, bf16* lut, cudaStream_t stream);
 
+// One thread waits on an mbarrier that never completes until limit_ns has
+// passed, then records DS_VIT_ETIMEOUT in *status; *elapsed = the time waited.
+int launch_selftest_wait(int* status, unsigned long long* elapsed, unsigned long long limit_ns,
+                         cudaStream_t stream);
+
 // The patch projection's K order inside the GEMM: patch row y fills columns
 // y*64 .. y*64+41 in pixel order (x*3 + c), columns y*64+42 .. y*64+63 are
 // zero.  The weight is permuted to match once at preparation; the product is

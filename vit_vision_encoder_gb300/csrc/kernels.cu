@@ -256,6 +256,30 @@ int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing
+// completes, gives up after limit_ns of %globaltimer, records the timeout in
+// *status as every kernel's bounded waits do, and stores how long it waited.
+__global__ void selftest_wait_kernel(int* status, unsigned long long* elapsed, unsigned long long limit_ns) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  fence_barrier_init();
+  const unsigned long long t0 = global_timer();
+  while (!mbar_try_wait(b, 0)) {
+    if (global_timer() - t0 > limit_ns) {
+      report_error(status, kErrTimeout);
+      break;
+    }
+  }
+  *elapsed = global_timer() - t0;
+}
+
+int launch_selftest_wait(int* status, unsigned long long* elapsed, unsigned long long limit_ns,
+                         cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 1, 0, stream>>>(status, elapsed, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
 int launch_pixel_lut(const PixelNorm& norm, bf16* lut, cudaStream_t stream) {
   pixel_lut_kernel<<<3, 256, 0, stream>>>(norm, lut);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;

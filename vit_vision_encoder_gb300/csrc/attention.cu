@@ -34,7 +34,6 @@
 #include "internal.h"
 #include "ptx.cuh"
 
-#include <mutex>
 
 namespace dsvit {
 
@@ -385,13 +384,7 @@ __global__ void __maxnreg__(96)
 
 int launch_attention(const CUtensorMap& tm_qkv, const AttnBatch& batch, bf16* out, int* status,
                      cudaStream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
+  if (allow_smem(reinterpret_cast<const void*>(attn_kernel), kSmemBytes) != cudaSuccess) return DS_VIT_ECUDA;
   AttnParams p;
   p.b = batch;
   p.out = out;

@@ -36,7 +36,6 @@
 #include "internal.h"
 #include "ptx.cuh"
 
-#include <mutex>
 
 namespace dsvit {
 
@@ -429,12 +428,7 @@ __global__ void __maxnreg__(96)
 
 int launch_attention_hd72(const CUtensorMap& tm_qkv, const CUtensorMap& tm_qkv_tail, int n, bf16* out,
                           int* status, cudaStream_t stream) {
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(attn_hd72_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  });
-  if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
+  if (allow_smem(reinterpret_cast<const void*>(attn_hd72_kernel), kSmemBytes) != cudaSuccess) return DS_VIT_ECUDA;
   if (n <= 0) return DS_VIT_OK;
   QwenAttnParams p;
   p.n = n;

@@ -31,6 +31,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <map>
 #include <mutex>
 
 namespace dsvit {
@@ -714,13 +715,8 @@ template <int BN, int EPI, int ASRC = kATma>
 int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
                   const GemmParams& p, cudaStream_t stream, const AGenParams* g = nullptr) {
   using C = GemmCfg<BN, ASRC>;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_kernel<BN, EPI, ASRC>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-  });
-  if (attr_err != cudaSuccess) return DS_VIT_ECUDA;
+  if (allow_smem(reinterpret_cast<const void*>(gemm_kernel<BN, EPI, ASRC>), C::SMEM_BYTES) != cudaSuccess)
+    return DS_VIT_ECUDA;
   const int tiles = ((p.M + 127) / 128) * (p.N / BN);
   const int grid = tiles < num_sms() ? tiles : num_sms();
   static const AGenParams none{};
@@ -759,6 +755,24 @@ bool encode_tmap(CUtensorMap* map, const void* base, uint64_t rows, uint64_t col
 }
 
 }  // namespace
+
+cudaError_t allow_smem(const void* kernel, int bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return cudaErrorInvalidDevice;
+  }
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, cudaError_t> done;
+  std::lock_guard<std::mutex> lock(mu);
+  const auto key = std::make_pair(kernel, dev);
+  const auto it = done.find(key);
+  if (it != done.end()) return it->second;
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e != cudaSuccess) cudaGetLastError();
+  done[key] = e;
+  return e;
+}
 
 int num_sms() {
   static int n = 0;

@@ -57,6 +57,11 @@ bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t 
 
 int num_sms();
 
+// Lets `kernel` use `bytes` of dynamic shared memory on the current device,
+// once per (kernel, device): a process that drives several GPUs sets it on
+// each.  Returns the result of that first cudaFuncSetAttribute.
+cudaError_t allow_smem(const void* kernel, int bytes);
+
 // TMA maps of one weight matrix B [N, K] for both GEMM tile widths.
 struct WeightMap {
   CUtensorMap bn256;   // box 256 rows

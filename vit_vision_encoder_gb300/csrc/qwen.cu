@@ -58,8 +58,11 @@ __global__ void qwen_patch_kernel(const uint8_t* __restrict__ pix, int W, int gw
 
 // x[r] = bf16(bilinear sample of the 48x48 table at the align-corners position
 // of patch (gy, gx)): y = gy*47/(gh-1) in float64, weights in fp32, products
-// and sums rounded one at a time in the oracle's order.
-__global__ void qwen_pos_kernel(const bf16* __restrict__ table, int gh, int gw, bf16* __restrict__ x) {
+// and sums rounded one at a time in the oracle's order.  One block of 144
+// threads per row, 8 consecutive dims a thread (16-byte loads and stores).
+constexpr int kPosThreads = kD / 8;
+__global__ void __launch_bounds__(kPosThreads) qwen_pos_kernel(const bf16* __restrict__ table, int gh, int gw,
+                                                               bf16* __restrict__ x) {
   const int r = blockIdx.x;
   int gy, gx;
   group_pos(r, gw, &gy, &gx);
@@ -70,15 +73,28 @@ __global__ void qwen_pos_kernel(const bf16* __restrict__ table, int gh, int gw, 
   const float fy = static_cast<float>(__dsub_rn(yv, static_cast<double>(y0)));
   const float fx = static_cast<float>(__dsub_rn(xv, static_cast<double>(x0)));
   const float ofy = __fsub_rn(1.f, fy), ofx = __fsub_rn(1.f, fx);
-  const bf16* t00 = table + static_cast<size_t>(y0 * 48 + x0) * kD;
-  const bf16* t01 = table + static_cast<size_t>(y0 * 48 + x1) * kD;
-  const bf16* t10 = table + static_cast<size_t>(y1 * 48 + x0) * kD;
-  const bf16* t11 = table + static_cast<size_t>(y1 * 48 + x1) * kD;
-  for (int d = threadIdx.x; d < kD; d += blockDim.x) {
-    const float top = __fadd_rn(__fmul_rn(__bfloat162float(t00[d]), ofx), __fmul_rn(__bfloat162float(t01[d]), fx));
-    const float bot = __fadd_rn(__fmul_rn(__bfloat162float(t10[d]), ofx), __fmul_rn(__bfloat162float(t11[d]), fx));
-    x[static_cast<size_t>(r) * kD + d] = __float2bfloat16_rn(__fadd_rn(__fmul_rn(top, ofy), __fmul_rn(bot, fy)));
+  const int d = threadIdx.x;   // 16-byte word of the row
+  auto row = [&](int ty, int tx) {
+    return __ldg(reinterpret_cast<const uint4*>(table + static_cast<size_t>(ty * 48 + tx) * kD) + d);
+  };
+  const uint4 a00 = row(y0, x0), a01 = row(y0, x1), a10 = row(y1, x0), a11 = row(y1, x1);
+  const uint32_t w00[4] = {a00.x, a00.y, a00.z, a00.w}, w01[4] = {a01.x, a01.y, a01.z, a01.w};
+  const uint32_t w10[4] = {a10.x, a10.y, a10.z, a10.w}, w11[4] = {a11.x, a11.y, a11.z, a11.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    float v[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      auto f = [&](uint32_t w) { return hh ? __uint_as_float(w & 0xFFFF0000u) : __uint_as_float(w << 16); };
+      const float top = __fadd_rn(__fmul_rn(f(w00[e]), ofx), __fmul_rn(f(w01[e]), fx));
+      const float bot = __fadd_rn(__fmul_rn(f(w10[e]), ofx), __fmul_rn(f(w11[e]), fx));
+      v[hh] = __fadd_rn(__fmul_rn(top, ofy), __fmul_rn(bot, fy));
+    }
+    __nv_bfloat162 pv = __floats2bfloat162_rn(v[0], v[1]);
+    o[e] = *reinterpret_cast<uint32_t*>(&pv);
   }
+  reinterpret_cast<uint4*>(x + static_cast<size_t>(r) * kD)[d] = make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 // [pos][j] = cos(pos * theta^(-j/18)), [pos][18 + j] = sin(...), double -> fp32.
@@ -380,7 +396,7 @@ int ds_vit_qwen_encode(const ds_vit_qwen_prepared* p, const uint8_t* pixels, int
 
   qwen_patch_kernel<<<N, 256, 0, st>>>(pixels, W, gw, p->pix_lut, h);
   qwen_rope_rows_kernel<<<(N * 40 + 255) / 256, 256, 0, st>>>(rope_rows, N, gw, p->rope_cs);
-  qwen_pos_kernel<<<N, 256, 0, st>>>(static_cast<const bf16*>(w.pos_table), gh, gw, x);
+  qwen_pos_kernel<<<N, kPosThreads, 0, st>>>(static_cast<const bf16*>(w.pos_table), gh, gw, x);
   QW_CUDA(cudaGetLastError());
   QW_TRY(launch_gemm(tA_pix, p->tm_patch, tC_x, N, kD, 1536, static_cast<const bf16*>(w.patch_b), x,
                      kEpiBiasResid, nullptr, nullptr, p->status, st));

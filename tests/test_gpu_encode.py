@@ -238,3 +238,19 @@ def test_overlay_rejects_out_of_range(dv, w32):
         dv.overlay(h, [(0, 6, 6, 0), (5, 6, 6, 0)], emb, s)   # overlapping spans
     torch.cuda.synchronize()
     assert bool((h == 0).all())
+
+
+def test_seeded_size_sweep(dv, enc2, w2):
+    """A seeded batch of irregular grids (ragged query and key tiles, grids that
+    are not multiples of 3, extreme aspects), at most ~4000 patches in all:
+    every step teacher-forced, the free-running output within the oracle's
+    spread, and the token offsets exact."""
+    rng = np.random.default_rng(4242)
+    sizes = [(1, 1), (3, 37)]
+    while sum(gh * gw for gh, gw in sizes) < 3000:
+        sizes.append((int(rng.integers(1, 41)), int(rng.integers(1, 41))))
+    imgs = [WL.uniform_image(14 * gh, 14 * gw, seed=500 + i) for i, (gh, gw) in enumerate(sizes)]
+    out, offs, blocks, fnorm = _run(dv, enc2, imgs, dump=True)
+    assert_steps_teacher_forced(imgs, w2, WL.MODEL, blocks, fnorm, out, layers=(0, 1))
+    ref_offs, _ = assert_end_to_end(host(out), imgs, w2, WL.MODEL, what=f"sweep {sizes}")
+    assert np.array_equal(offs, ref_offs)

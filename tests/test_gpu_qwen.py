@@ -146,3 +146,30 @@ def test_qwen_peaked_attention(dv, wq):
         assert_parity(bits_of(bl[1]), ref, what="peaked block 0")
     finally:
         e.close()
+
+
+@pytest.mark.parametrize("H,W", [(32, 32), (96, 1024), (736, 416)])
+def test_qwen_irregular_grids(dv, wq, H, W):
+    """Grids of 2x2 (one merge group), 6x64 and 46x26 patches (ragged query
+    and key tiles, N = 4, 384, 1196): the patch embedding and two blocks
+    teacher-forced, and the merger of the second block's output."""
+    cfg = WL.QWEN_MODEL
+    e = dv.QwenEncoder(dv.weights_to_device(wq), cfg, n_layers=2)
+    try:
+        img = WL.uniform_image(H, W, seed=700 + H)
+        out, _, blocks = e.encode(torch.from_numpy(img).cuda(), deepstack=False, dump=True)
+        torch.cuda.synchronize()
+        bl = blocks.cpu()
+        gh, gw = H // 16, W // 16
+        gy, gx = Q.patch_order(gh, gw)
+        A = Q.patchify(img, cfg["mean"], cfg["std"])
+        pos = Q.pos_interp(wq["pos_table"], gh, gw).reshape(gh, gw, -1)[gy, gx]
+        x0 = O.round_bf16(O.round_bf16(pos) + (O.mm(A, O.bits_to_f32(wq["patch_w"]).T) +
+                                              O.bits_to_f32(wq["patch_b"])))
+        assert_parity(bits_of(bl[0]), x0, what="patch embedding")
+        for l in range(2):
+            ref = Q.block(bits_of(bl[l]), wq["layers"][l], cfg, gy, gx)
+            assert_parity(bits_of(bl[l + 1]), ref, what=f"block {l}")
+        assert_parity(host(out), Q.merger(bits_of(bl[2]), wq["merger"], cfg), what="merger")
+    finally:
+        e.close()

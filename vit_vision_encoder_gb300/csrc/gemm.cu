@@ -185,7 +185,6 @@ __device__ __forceinline__ void produce_a_merge(const AGenParams& g, const GemmP
     // the window positions inside the grid (bit p).
     int base[8];
     uint32_t geo[8];
-#pragma unroll
     const int64_t row0 = static_cast<int64_t>(tile_mb(tile, num_m, num_n, p.n_fast)) * C::BM;
     for (int q = 0; q < 8; ++q) {
       const int64_t row = row0 + q * 16 + (t >> 3);

@@ -39,7 +39,8 @@ def test_rmsnorm(dv):
         assert (got == ref).mean() > 0.99
 
 
-@pytest.mark.parametrize("M,K,F", [(1, 64, 128), (300, 1024, 512), (1000, 1024, 4096), (2000, 256, 1024)])
+@pytest.mark.parametrize("M,K,F", [(1, 64, 128), (300, 1024, 512), (1000, 1024, 4096), (2000, 256, 1024),
+                                   (2000, 2048, 1024)])
 def test_linear_swiglu(dv, M, K, F):
     a = rand_bits((M, K), 53 + M)
     w = rand_bits((2 * F, K), 54 + K, 1.0 / math.sqrt(K))

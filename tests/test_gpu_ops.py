@@ -55,6 +55,11 @@ GEMM_CASES = [
     # N % 256 == 128 with many rows (N = 1152 is the Qwen-style tower's hidden
     # width; 128-wide tiles, ragged M in the second case).
     (4096, 1152, 1152, "resid"), (3000, 1152, 1152, "bias"), (2500, 640, 1408, "gelu"),
+    # K >= 2048 with enough 256 x 256 tiles: the 2-CTA-cluster kernel.  FC2-like
+    # K = 4096; M = 4200, whose last tile's second 128-row half lies wholly past
+    # M; the second merger linear's K = N = 5120.
+    (3840, 4096, 1024, "resid"), (4200, 2048, 1024, "gelu"), (4200, 4096, 1024, "resid"),
+    (1024, 5120, 5120, "bias"),
 ]
 
 
@@ -113,7 +118,7 @@ def test_gelu_epilogue_every_bf16_input(dv):
     assert (ulps == 0).mean() > 0.995
 
 
-@pytest.mark.parametrize("gh,gw", [(6, 6), (25, 21), (192, 2)])
+@pytest.mark.parametrize("gh,gw", [(6, 6), (25, 21), (192, 2), (64, 80)])
 def test_linear_qkv_rope(dv, gh, gw):
     M = gh * gw
     cfg = WL.MODEL

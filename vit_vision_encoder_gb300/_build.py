@@ -10,7 +10,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsvit.so")
-SOURCES = ("api.cu", "gemm.cu", "attention.cu", "attention_qwen.cu", "kernels.cu", "noalloc.cu",
+SOURCES = ("api.cu", "gemm.cu", "gemm_pair.cu", "attention.cu", "attention_qwen.cu", "kernels.cu", "noalloc.cu",
            "preprocess.cu", "qwen.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -34,7 +34,7 @@ def _newer(target: str, deps) -> bool:
 def build(verbose: bool = False, ptxas_info: bool = False) -> str:
     """Compile every .cu (in parallel) and link libdsvit.so.  Returns its path."""
     os.makedirs(BUILD, exist_ok=True)
-    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
+    headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh", ".inc"))]
     headers.append(os.path.join(os.path.dirname(PKG), "include", "dsvit.h"))
     objs, jobs = [], []
     for src in SOURCES:

@@ -38,19 +38,7 @@ namespace dsvit {
 
 namespace {
 
-struct GemmParams {
-  int M, N, K;
-  bf16* out;          // read by the residual epilogue; written through tmC
-  const bf16* bias;
-  const int* rowpos;
-  const float* rope_cs;
-  int* status;
-  int n_fast;         // tile order: 1 = n-block fastest, 0 = m-block fastest
-};
-
-// n-block-fastest order when the A operand would not stay in L2 between the
-// passes over its n-blocks.
-int tile_order(int64_t M, int K) { return M * K * 2 > (int64_t{40} << 20) ? 1 : 0; }
+#include "gemm_common.cuh"
 
 template <int BN, int ASRC = kATma>
 struct GemmCfg {
@@ -85,75 +73,6 @@ static_assert(GemmCfg<128>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<256, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(3 * GemmCfg<128>::STAGES + 5 <= 31, "barrier slots");
-
-// GELU(x) = x Phi(x), Phi from erf ("End-to-end results and their limits":
-// the erf form).  erf by Abramowitz & Stegun 7.1.26 (Hastings): for z >= 0,
-// erfc(z) ~ q = t (a1 + t (a2 + t (a3 + t (a4 + t a5)))) exp(-z^2) with
-// t = 1 / (1 + p z), |erf error| <= 1.5e-7; then 2 Phi(x) = 2 - q for x >= 0
-// and q for x < 0 (z = |x| / sqrt 2), so the negative tail keeps its relative
-// precision.  Over [-10, 10] the GELU error is below 2.2e-7 absolute and
-// 1.7e-4 relative wherever |GELU| > 1e-3.  Two elements per call, on packed
-// f32x2 arithmetic; reciprocal and exp2 are the MUFU approximations.
-__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float& lo, float& hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-__device__ __forceinline__ void gelu_erf2(float& x0, float& x1) {
-  const float kP = 0.3275911f;
-  const uint64_t a5 = pk2(1.061405429f, 1.061405429f), a4 = pk2(-1.453152027f, -1.453152027f);
-  const uint64_t a3 = pk2(1.421413741f, 1.421413741f), a2 = pk2(-0.284496736f, -0.284496736f);
-  const uint64_t a1 = pk2(0.254829592f, 0.254829592f);
-  const float z0 = fabsf(x0) * 0.70710678118654752f, z1 = fabsf(x1) * 0.70710678118654752f;
-  const uint64_t z = pk2(z0, z1);
-  float d0, d1;
-  upk2(fma2(pk2(kP, kP), z, pk2(1.f, 1.f)), d0, d1);
-  const uint64_t t = pk2(rcp_approx(d0), rcp_approx(d1));
-  uint64_t poly = fma2(a5, t, a4);
-  poly = fma2(poly, t, a3);
-  poly = fma2(poly, t, a2);
-  poly = fma2(poly, t, a1);
-  poly = mul2(poly, t);
-  float w0, w1;   // -z^2 log2(e)
-  upk2(mul2(mul2(z, z), pk2(-1.4426950408889634f, -1.4426950408889634f)), w0, w1);
-  float q0, q1;
-  upk2(mul2(poly, pk2(ex2_approx(w0), ex2_approx(w1))), q0, q1);
-  const float p0 = x0 >= 0.f ? 2.f - q0 : q0, p1 = x1 >= 0.f ? 2.f - q1 : q1;   // 2 Phi
-  float g0, g1;
-  upk2(mul2(mul2(pk2(x0, x1), pk2(0.5f, 0.5f)), pk2(p0, p1)), g0, g1);
-  x0 = g0;
-  x1 = g1;
-}
-
-// Tile order.  n-block fastest: the CTAs resident at one time cover few row
-// blocks of A, each read from DRAM once and shared through L2 by all the
-// n-blocks of its row (m-block-fastest order re-read the 75 MB A of the FC2
-// shape from DRAM once per n-block column).  m-block fastest: the resident
-// CTAs share few B tiles, which suits an A that stays in L2 anyway.
-__device__ __forceinline__ int tile_mb(int tile, int num_m, int num_n, int n_fast) {
-  return n_fast ? tile / num_n : tile % num_m;
-}
-__device__ __forceinline__ int tile_nb(int tile, int num_m, int num_n, int n_fast) {
-  return n_fast ? tile % num_n : tile / num_m;
-}
 
 // Image of packed row `row` (offsets `off`, n images) and the row's index in it.
 __device__ __forceinline__ int find_image(const int64_t* off, int n, int64_t row, int* local) {
@@ -502,195 +421,15 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-7)
-    const int grp = warp >> 2;                   // chunk parity this warp handles
-    const int quad = warp & 3;                   // TMEM lane quadrant = 32-row slice
-    const uint32_t lane_sel = static_cast<uint32_t>(quad * 32) << 16;
-    const uint32_t stg0 = smem_u32(smem + C::OFF_STG + warp * 2 * C::STG_BYTES);
-    const uint32_t bias_s = smem_u32(smem + C::OFF_BIAS);
-    uint32_t acc = 0, acc_phase = 0;
-    int stg = 0, it = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++it) {
-      const int mb = tile_mb(tile, num_m, num_n, p.n_fast), nb = tile_nb(tile, num_m, num_n, p.n_fast);
-      // The tile's bias -> shared memory (buffer it & 1), by warp 0.
-      const uint32_t bias_buf = bias_s + (it & 1) * (BN * 2);
-      if (warp == 0) {
-#pragma unroll
-        for (int q = lane; q < BN / 8; q += 32) {
-          // SwiGLU: gate biases in the first half of the buffer, up biases in the second.
-          const bf16* bsrc = EPI == kEpiSwiglu
-                                 ? (q < BN / 16 ? p.bias + nb * (BN / 2) : p.bias + p.N / 2 + nb * (BN / 2) - BN / 2)
-                                 : p.bias + nb * BN;
-          const uint4 b = __ldg(reinterpret_cast<const uint4*>(bsrc) + q);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(bias_buf + q * 16), "r"(b.x),
-                       "r"(b.y), "r"(b.z), "r"(b.w)
-                       : "memory");
-        }
-      }
-      named_barrier(1, C::EPI_WARPS * 32);
-      const int row0 = mb * C::BM + quad * 32;
-      const int row = row0 + lane;
-      const bool valid = row < p.M;
-      // RoPE: warps of group 0 hold head dims 0..31 (patch row), group 1 dims
-      // 32..63 (patch column); all columns of a tile below 2048 are q or k.
-      float rc[16], rs[16];
-      bool rotate = false;
-      if constexpr (EPI == kEpiQkvRope) {
-        rotate = nb * BN < 2048;
-        if (rotate) {
-          int pos = 0;
-          if (valid) {
-            const int rp = __ldg(p.rowpos + row);
-            pos = grp == 0 ? (rp >> 16) : (rp & 0xFFFF);
-          }
-          const float4* cs = reinterpret_cast<const float4*>(p.rope_cs + pos * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 a = __ldg(cs + q), b = __ldg(cs + 4 + q);
-            rc[4 * q] = a.x; rc[4 * q + 1] = a.y; rc[4 * q + 2] = a.z; rc[4 * q + 3] = a.w;
-            rs[4 * q] = b.x; rs[4 * q + 1] = b.y; rs[4 * q + 2] = b.z; rs[4 * q + 3] = b.w;
-          }
-        }
-      }
-      // Residual: every chunk of this warp's rows is loaded before the
-      // accumulator wait, so the loads overlap the tile's main loop.
-      uint4 rxa[EPI == kEpiBiasResid ? BN / 64 : 1][4];
-      if constexpr (EPI == kEpiBiasResid) {
-#pragma unroll
-        for (int cc = 0; cc < BN / 64; ++cc) {
-          const uint4* src = reinterpret_cast<const uint4*>(
-              p.out + static_cast<size_t>(row) * p.N + nb * BN + (2 * cc + grp) * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) rxa[cc][q] = valid ? src[q] : make_uint4(0, 0, 0, 0);
-        }
-      }
-      if (!mbar_wait(tfull_bar(acc), acc_phase, p.status)) break;
-      tc_fence_after();
-      // Output chunks of 32 columns per warp; SwiGLU tiles output BN/2 columns.
-      constexpr int kChunks = EPI == kEpiSwiglu ? BN / 128 : BN / 64;
-#pragma unroll
-      for (int cc = 0; cc < kChunks; ++cc) {
-        const int c = 2 * cc + grp;
-        const int n0 = (EPI == kEpiSwiglu ? nb * (BN / 2) : nb * BN) + c * 32;
-        uint4 rx[4];
-        if constexpr (EPI == kEpiBiasResid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) rx[q] = rxa[cc][q];
-        }
-        uint32_t r[32];
-        uint32_t ru[EPI == kEpiSwiglu ? 32 : 1];
-        tmem_ld32(tmem_base + acc * BN + c * 32 + lane_sel, r);
-        if constexpr (EPI == kEpiSwiglu) tmem_ld32(tmem_base + acc * BN + BN / 2 + c * 32 + lane_sel, ru);
-        tmem_wait_ld();
-        if (cc == kChunks - 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(tempty_bar(acc));
-        }
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          uint32_t bw[4];
-          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                       : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
-                       : "r"(bias_buf + c * 64 + q * 16));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            v[q * 8 + 2 * e] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e]), bf16lo(bw[e]));
-            v[q * 8 + 2 * e + 1] = __fadd_rn(__uint_as_float(r[q * 8 + 2 * e + 1]), bf16hi(bw[e]));
-          }
-        }
-        if constexpr (EPI == kEpiBiasGelu) {
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) gelu_erf2(v[i], v[i + 1]);
-        } else if constexpr (EPI == kEpiSwiglu) {
-          // v = gate + b_gate; out = silu(v) * (up + b_up), silu(v) = v / (1 + 2^(-v log2 e)).
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t bw[4];
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(bw[0]), "=r"(bw[1]), "=r"(bw[2]), "=r"(bw[3])
-                         : "r"(bias_buf + BN + c * 64 + q * 16));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const int i = q * 8 + 2 * e + hh;
-                const float u = __fadd_rn(__uint_as_float(ru[i]), hh ? bf16hi(bw[e]) : bf16lo(bw[e]));
-                const float den = __fadd_rn(1.f, ex2_approx(__fmul_rn(v[i], -1.4426950408889634f)));
-                v[i] = __fmul_rn(__fmul_rn(v[i], rcp_approx(den)), u);
-              }
-            }
-          }
-        } else if constexpr (EPI == kEpiBiasResid) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint32_t xw[4] = {rx[q].x, rx[q].y, rx[q].z, rx[q].w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              v[q * 8 + 2 * e] = __fadd_rn(bf16lo(xw[e]), v[q * 8 + 2 * e]);
-              v[q * 8 + 2 * e + 1] = __fadd_rn(bf16hi(xw[e]), v[q * 8 + 2 * e + 1]);
-            }
-          }
-        } else if constexpr (EPI == kEpiQkvRope72) {
-          // q and k: r(rot(r(t))).  Each 16-column group holds 8 rotation
-          // pairs (i, i + 8); rope_cs[row][slot] = (cos, sin) of pair slot
-          // 8 g + i of group g = (column mod 80) / 16.
-          if (n0 < kQwenQkCols && valid) {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
-            const float4* rt = reinterpret_cast<const float4*>(p.rope_cs + static_cast<size_t>(row) * 80);
-#pragma unroll
-            for (int t = 0; t < 2; ++t) {
-              const int g = ((n0 + 16 * t) % 80) / 16;
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                const float4 cs = __ldg(rt + 4 * g + q);    // slots 2q, 2q + 1 of the group
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                  const int i = 16 * t + 2 * q + e;
-                  const float co = e ? cs.z : cs.x, si = e ? cs.w : cs.y;
-                  const float a = v[i], b = v[i + 8];
-                  v[i] = __fsub_rn(__fmul_rn(a, co), __fmul_rn(b, si));
-                  v[i + 8] = __fadd_rn(__fmul_rn(b, co), __fmul_rn(a, si));
-                }
-              }
-            }
-          }
-        } else if constexpr (EPI == kEpiQkvRope) {
-          if (rotate) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float a = v[j], b = v[j + 16];
-              v[j] = __fsub_rn(__fmul_rn(a, rc[j]), __fmul_rn(b, rs[j]));
-              v[j + 16] = __fadd_rn(__fmul_rn(b, rc[j]), __fmul_rn(a, rs[j]));
-            }
-          }
-        }
-        // Stage the 32x32 chunk (64-byte swizzle: 16-byte unit q of row r at
-        // unit q ^ ((r >> 1) & 3)) and store it with TMA.
-        const uint32_t buf = stg0 + stg * C::STG_BYTES;
-        if (lane == 0) bulk_wait_read<1>();        // this buffer's previous store has read it
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t addr = buf + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
-                       "r"(pack_bf16x2(v[q * 8 + 0], v[q * 8 + 1])), "r"(pack_bf16x2(v[q * 8 + 2], v[q * 8 + 3])),
-                       "r"(pack_bf16x2(v[q * 8 + 4], v[q * 8 + 5])), "r"(pack_bf16x2(v[q * 8 + 6], v[q * 8 + 7]))
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0 && row0 < p.M) {
-          tma_store_2d(&tmC, buf, n0, row0);
-          bulk_commit();
-        }
-        stg ^= 1;
-      }
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
-    }
-    if (lane == 0) bulk_wait_all();
+#define GEMM_FIRST_TILE blockIdx.x
+#define GEMM_TILE_STEP gridDim.x
+#define GEMM_ROW0 mb * C::BM + quad * 32
+#define GEMM_RELEASE_ACC mbar_arrive(tempty_bar(acc))
+#include "gemm_epilogue.inc"
+#undef GEMM_FIRST_TILE
+#undef GEMM_TILE_STEP
+#undef GEMM_ROW0
+#undef GEMM_RELEASE_ACC
   }
 
   tc_fence_before();
@@ -811,6 +550,13 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
                 int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 128 != 0) return DS_VIT_EINVAL;
+  // Long K where 256-wide tiles keep the SMs busy: 256 x 256 tiles on 2-CTA
+  // clusters (a third less operand traffic per stage and six stages).  At
+  // K = 1024 the pair's coupled pipelines lost to one-CTA tiles.
+  if (N % 256 == 0 && K >= 2048 && gemm_bn(M, N) == 256) {
+    const int rc = launch_gemm_pair(tmA, B.bn128, tmC, M, N, K, bias, out, epi, rowpos, rope_cs, status, stream);
+    if (rc != kGemmNoPair) return rc;
+  }
   GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status, tile_order(M, K)};
   // SwiGLU pairs the gate and up halves of one 256-column tile (two 128-row B boxes).
   if (epi == kEpiSwiglu) {

@@ -80,6 +80,15 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
 // than a quarter of the SMs idle (small M).
 int gemm_bn(int M, int N);
 
+// out[M, N] = epi(A B^T + bias) in 256 x 256 tiles on 2-CTA clusters
+// (tcgen05 cta_group::2; gemm_pair.cu); B through its 128-row-box map.  N a
+// multiple of 256.  Returns kGemmNoPair, launching nothing, when no cluster of
+// two such CTAs fits on the device.
+constexpr int kGemmNoPair = 1;
+int launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB128, const CUtensorMap& tmC, int M, int N,
+                     int K, const bf16* bias, bf16* out, int epi, const int* rowpos, const float* rope_cs,
+                     int* status, cudaStream_t stream);
+
 // Query rows per attention CTA (two 128-row tiles).
 constexpr int kAttnRowsPerCta = 256;
 

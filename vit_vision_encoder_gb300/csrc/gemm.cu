@@ -26,6 +26,8 @@
 // the main loop of the next.  The tile's bias is staged once in shared memory;
 // each 32x32 output chunk goes through a 64-byte-swizzled shared staging tile
 // (two per warp) and leaves by TMA store, which also clips rows past M.
+// Long-K GEMMs with 256-wide tiles go to the 2-CTA-cluster kernel instead
+// (gemm_pair.cu, 256 x 256 tiles, same epilogue source).
 #include "internal.h"
 #include "ptx.cuh"
 

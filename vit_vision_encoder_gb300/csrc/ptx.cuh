@@ -398,12 +398,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
-__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cbar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar),
-               "r"(bytes)
-               : "memory");
-}
-
 // TMA tile load into this CTA's shared memory whose completion is signalled on
 // an mbarrier of either CTA of the pair (cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t cbar, int x,

@@ -26,8 +26,10 @@
 // the main loop of the next.  The tile's bias is staged once in shared memory;
 // each 32x32 output chunk goes through a 64-byte-swizzled shared staging tile
 // (two per warp) and leaves by TMA store, which also clips rows past M.
-// Long-K GEMMs with 256-wide tiles go to the 2-CTA-cluster kernel instead
-// (gemm_pair.cu, 256 x 256 tiles, same epilogue source).
+// Where 256-wide tiles are chosen and A comes by TMA, the 2-CTA-cluster
+// kernel runs instead (gemm_pair.cu, 256 x 256 tiles, same epilogue source);
+// this kernel keeps 128-wide tiles, the produced-A GEMMs and devices where no
+// pair of its CTAs fits.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -552,10 +554,9 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
                 int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 128 != 0) return DS_VIT_EINVAL;
-  // Long K where 256-wide tiles keep the SMs busy: 256 x 256 tiles on 2-CTA
-  // clusters (a third less operand traffic per stage and six stages).  At
-  // K = 1024 the pair's coupled pipelines lost to one-CTA tiles.
-  if (N % 256 == 0 && K >= 2048 && gemm_bn(M, N) == 256) {
+  // Where 256-wide tiles keep the SMs busy: 256 x 256 tiles on 2-CTA clusters
+  // (a third less operand traffic per stage, six stages).
+  if (N % 256 == 0 && gemm_bn(M, N) == 256) {
     const int rc = launch_gemm_pair(tmA, B.bn128, tmC, M, N, K, bias, out, epi, rowpos, rope_cs, status, stream);
     if (rc != kGemmNoPair) return rc;
   }

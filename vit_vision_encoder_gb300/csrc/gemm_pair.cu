@@ -1,7 +1,7 @@
-// tcgen05 GEMM on 2-CTA clusters (cta_group::2) for the long-K contractions
-// (MLP down-projection K = 4096, second merger linear K = 5120): out =
-// epi(A B^T + bias) in 256 x 256 tiles, the same epilogues as the one-CTA
-// kernel (gemm.cu).
+// tcgen05 GEMM on 2-CTA clusters (cta_group::2) for the dense contractions
+// with 256-wide tiles and a TMA-loaded A (the encode's QKV, out-projection,
+// MLP and second merger linears): out = epi(A B^T + bias) in 256 x 256 tiles,
+// the same epilogues as the one-CTA kernel (gemm.cu).
 //
 // A tile's 256 rows are split between the two CTAs of the pair (128 each) and
 // so are its 256 B rows: each CTA stages by TMA its own 128 x 64 A and 128 x 64

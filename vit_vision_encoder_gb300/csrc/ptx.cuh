@@ -393,9 +393,12 @@ __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
 }
 
-// Arrive on an mbarrier given by its cluster address (possibly the peer's).
+// Arrive on an mbarrier given by its cluster address (possibly the peer's),
+// with the default (CTA-scope release) semantics: it signals TMEM reads that
+// tcgen05.wait::ld and tcgen05.fence::before_thread_sync already ordered; a
+// cluster-scope release here cost the epilogue microseconds per tile.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 
 // TMA tile load into this CTA's shared memory whose completion is signalled on

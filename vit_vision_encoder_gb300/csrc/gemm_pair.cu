@@ -16,7 +16,9 @@
 //   tempty[a] (leader)  all 16 epilogue warps of the pair have read it;
 //   drain     (each)    the leader's last MMAs are done (TMEM, operands free).
 // The pair meets at cluster barriers after the barrier initialisation and
-// before the collective TMEM release.  Every mbarrier wait is bounded.
+// before the collective TMEM release.  No arrival inside the loops carries a
+// cluster-scope release: one per stage halved the kernel's speed, one per
+// tile cost microseconds.  Every mbarrier wait is bounded.
 #include "internal.h"
 #include "ptx.cuh"
 

@@ -253,11 +253,17 @@ int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* con
  *   Same arguments and results as ds_vit_encode, without ws/ws_bytes: the
  *   scratch is a file-scope device array of DS_VIT_NOALLOC_SCRATCH_BYTES
  *   inside the library, held by every GPU that loads the library until exit.
- *   Images over DS_VIT_NOALLOC_MAX_PATCHES patches return DS_VIT_ERANGE (after
- *   the usual DS_VIT_EINVAL checks) and nothing is written.
- *   The call allocates and frees nothing.  Its first call on a device looks up
- *   the array's device address on that device (cudaGetSymbolAddress, with the
- *   device current); make that first call before any stream capture.
+ *   Checks, in this order, each failing before anything is written:
+ *   DS_VIT_EINVAL for a null pointer, `out` not 16-byte or `pixels` not
+ *   4-byte aligned, or H / W not positive multiples of 14; DS_VIT_ERANGE for
+ *   an image over the ds_vit_encode limits; DS_VIT_EINVAL when the current
+ *   device is not the one `p` was prepared on; DS_VIT_ERANGE for an image
+ *   over DS_VIT_NOALLOC_MAX_PATCHES patches.
+ *   The call allocates and frees nothing.  The array's device address belongs
+ *   to the current CUDA context: the first call in each context (a device's
+ *   primary context, again after cudaDeviceReset, or a context the caller
+ *   created) looks it up with cudaGetSymbolAddress, with the device current;
+ *   make that first call before any stream capture.
  *   All calls share the array and it keeps the last call's contents (no part
  *   needs to start at zero); calls whose kernels overlap on the GPU race.
  */
@@ -294,6 +300,37 @@ int ds_vit_encode_debug(const ds_vit_prepared* p, int n, const uint8_t* const* p
 int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_span* spans,
                    int n_spans, const void* embeds, int64_t n_embeds, const void* sentinel,
                    void* stream);
+
+/*
+ * ds_vit_overlay_rows: the overlay driven by caller-given per-row arrays
+ * ([A] "Connect the complete image-to-text path first": IMAGE rows take
+ * aligner rows, START / NEWLINE / END rows the learned vectors; [A]'s routing
+ * section: the rows travel with their type).  For entry i < n:
+ *   hidden[rows[i]] = type[i] == IMAGE ? embeds[src[i]] : sentinel[START/NEWLINE/END].
+ * This form places rows anywhere (a non-contiguous placeholder layout, spans
+ * already interleaved with text by the caller); ds_vit_overlay is the compact
+ * form for contiguous spans.
+ *   hidden:  device bf16 [n_hidden, width]; width a multiple of 8.
+ *   rows, src: device int32 [n]; type: device uint8 [n] (DS_VIT_TOK_*), as
+ *            written by ds_vit_layout (rows = the destination rows, e.g. the
+ *            layout's pos when positions equal prompt rows).  src is read only
+ *            for IMAGE entries.  Rows must be distinct (two entries naming one
+ *            row leave either one's value).
+ *   embeds:  device bf16 [n_embeds, width]; sentinel: device bf16 [3, width].
+ *   status:  device int32, 0 on entry.  The entries live on the device, so
+ *            they are checked there, all of them before any row is written:
+ *            a type above DS_VIT_TOK_END records DS_VIT_EINVAL, a row outside
+ *            [0, n_hidden) or an IMAGE src outside [0, n_embeds) records
+ *            DS_VIT_ERANGE, and then nothing is written.  Read it after the
+ *            stream's work completes; a nonzero value left in it also stops
+ *            later calls from writing.
+ * Returns DS_VIT_EINVAL for null or misaligned pointers (rows, src, status
+ * 4-byte; hidden, embeds, sentinel 16-byte) or bad sizes, before any launch.
+ * Exact copy (bit-for-bit); rows not listed are not touched.
+ */
+int ds_vit_overlay_rows(void* hidden, int64_t n_hidden, int32_t width, const int32_t* rows,
+                        const uint8_t* type, const int32_t* src, int64_t n, const void* embeds,
+                        int64_t n_embeds, const void* sentinel, int32_t* status, void* stream);
 
 /*
  * ds_vit_overlay_chunk: the overlay for chunked prefill ([A] "Connect the

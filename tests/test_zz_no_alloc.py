@@ -81,5 +81,9 @@ def test_no_alloc_rejects_images_over_the_limit(dv, enc):
     rc = dv.lib.ds_vit_encode_noalloc(enc.handle, _p(img), 462, 462, _p(out), _stream())
     assert rc == dv.ERANGE
     assert dv.lib.ds_vit_encode_noalloc(enc.handle, _p(img), 463, 462, _p(out), _stream()) == dv.EINVAL
+    # A misaligned output is reported as such even for an image over the limit:
+    # the alignment checks come before the patch limit.
+    odd = C.c_void_p(out.data_ptr() + 2)
+    assert dv.lib.ds_vit_encode_noalloc(enc.handle, _p(img), 462, 462, odd, _stream()) == dv.EINVAL
     torch.cuda.synchronize()
     assert bool((out == 3.0).all())

@@ -93,6 +93,7 @@ SIGNATURES = {
     "ds_vit_encode_debug": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,
                                       _VP, _SZ, _VP, _VP, _VP]),
     "ds_vit_overlay": (C.c_int, [_VP, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP, _VP]),
+    "ds_vit_overlay_rows": (C.c_int, [_VP, _I64, _I32, _VP, _VP, _VP, _I64, _VP, _I64, _VP, _VP, _VP]),
     "ds_vit_overlay_chunk": (C.c_int, [_VP, _I64, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP,
                                        _VP, _VP]),
     "ds_vit_device_status": (C.c_int, [_VP, _VP]),
@@ -425,6 +426,21 @@ def overlay(hidden, spans, embeds, sentinel):
     check(lib.ds_vit_overlay(_ptr(hidden), hidden.shape[0], hidden.shape[1], arr, len(spans),
                              _ptr(embeds), embeds.shape[0], _ptr(sentinel), _stream()),
           "ds_vit_overlay")
+
+
+def overlay_rows(hidden, rows, types, src, embeds, sentinel, status=None):
+    """Per-row overlay (ds_vit_overlay_rows), in place on ``hidden``: rows and
+    src int32 CUDA tensors [n], types a uint8 CUDA tensor [n].  Entries are
+    checked on the device; ``status`` (an int32 CUDA tensor [1], zeroed here
+    when not given) receives the first error code.  Returns ``status``."""
+    torch = _torch()
+    if status is None:
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    check(lib.ds_vit_overlay_rows(_ptr(hidden), hidden.shape[0], hidden.shape[1], _ptr(rows), _ptr(types),
+                                  _ptr(src), rows.shape[0], _ptr(embeds), embeds.shape[0], _ptr(sentinel),
+                                  _ptr(status), _stream()),
+          "ds_vit_overlay_rows")
+    return status
 
 
 def overlay_chunk(chunk, chunk_begin, spans, embeds, sentinel, row_type=None):

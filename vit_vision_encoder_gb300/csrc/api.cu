@@ -321,6 +321,8 @@ int build_spans(const ds_vit_span* spans, int n_spans, int64_t n_embeds, int64_t
 
 }  // namespace
 
+int dsvit::prepared_device(const ds_vit_prepared* p) { return p->device; }
+
 extern "C" {
 
 const char* ds_vit_strerror(int code) {
@@ -518,6 +520,22 @@ int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_s
   DSV_TRY(build_spans(spans, n_spans, n_embeds, n_hidden, &os));
   return launch_overlay(static_cast<bf16*>(hidden), width, os, static_cast<const bf16*>(embeds),
                         static_cast<const bf16*>(sentinel), static_cast<cudaStream_t>(stream));
+}
+
+int ds_vit_overlay_rows(void* hidden, int64_t n_hidden, int32_t width, const int32_t* rows,
+                        const uint8_t* type, const int32_t* src, int64_t n, const void* embeds,
+                        int64_t n_embeds, const void* sentinel, int32_t* status, void* stream) {
+  if (!hidden || !rows || !type || !src || !embeds || !sentinel || !status || width <= 0 ||
+      width % 8 != 0 || n_hidden <= 0 || n_hidden > INT32_MAX || n < 0 || n > INT32_MAX ||
+      n_embeds < 0 || n_embeds > INT32_MAX)
+    return DS_VIT_EINVAL;
+  if (!aligned16(hidden) || !aligned16(embeds) || !aligned16(sentinel) ||
+      (reinterpret_cast<uintptr_t>(rows) & 3) || (reinterpret_cast<uintptr_t>(src) & 3) ||
+      (reinterpret_cast<uintptr_t>(status) & 3))
+    return DS_VIT_EINVAL;
+  return launch_overlay_rows(static_cast<bf16*>(hidden), n_hidden, width, rows, type, src, n,
+                             static_cast<const bf16*>(embeds), n_embeds, static_cast<const bf16*>(sentinel),
+                             reinterpret_cast<int*>(status), static_cast<cudaStream_t>(stream));
 }
 
 int ds_vit_overlay_chunk(void* chunk, int64_t chunk_begin, int64_t chunk_rows, int32_t width,

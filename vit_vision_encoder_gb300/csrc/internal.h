@@ -57,6 +57,10 @@ bool make_tmap_store_bf16(CUtensorMap* map, void* base, uint64_t rows, uint64_t 
 
 int num_sms();
 
+// The device a prepared model was built on (its weights, tensor maps and
+// status word live there).
+int prepared_device(const ds_vit_prepared* p);
+
 // Lets `kernel` use `bytes` of dynamic shared memory on the current device,
 // once per (kernel, device): a process that drives several GPUs sets it on
 // each.  Returns the result of that first cudaFuncSetAttribute.
@@ -183,5 +187,9 @@ int launch_overlay(bf16* hidden, int width, const OverlaySpans& spans, const bf1
 int launch_overlay_chunk(bf16* chunk, int64_t chunk_begin, int64_t chunk_rows, int width,
                          const OverlaySpans& spans, const bf16* embeds, const bf16* sentinel,
                          uint8_t* row_type, cudaStream_t stream);
+
+int launch_overlay_rows(bf16* hidden, int64_t n_hidden, int width, const int32_t* rows, const uint8_t* type,
+                        const int32_t* src, int64_t n, const bf16* embeds, int64_t n_embeds, const bf16* sentinel,
+                        int* status, cudaStream_t stream);
 
 }  // namespace dsvit

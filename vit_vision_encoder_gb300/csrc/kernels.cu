@@ -238,6 +238,44 @@ __global__ void __launch_bounds__(128) overlay_chunk_kernel(bf16* __restrict__ c
   for (int k = threadIdx.x; k < width / 8; k += blockDim.x) d4[k] = s4[k];
 }
 
+// Overlay from caller-given per-row arrays (rows, type, src on the device).
+// The entries are checked on the device before any row is written: the check
+// kernel records the first error in *status, and the copy kernel, launched
+// after it on the same stream, writes nothing while *status holds one.
+__global__ void __launch_bounds__(256) overlay_rows_check_kernel(const int32_t* __restrict__ rows,
+                                                                 const uint8_t* __restrict__ type,
+                                                                 const int32_t* __restrict__ src, int64_t n,
+                                                                 int64_t n_hidden, int64_t n_embeds,
+                                                                 int* __restrict__ status) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const int t = type[i];
+  int err = 0;
+  if (t > DS_VIT_TOK_END)
+    err = DS_VIT_EINVAL;
+  else if (rows[i] < 0 || rows[i] >= n_hidden || (t == DS_VIT_TOK_IMAGE && (src[i] < 0 || src[i] >= n_embeds)))
+    err = DS_VIT_ERANGE;
+  if (err) atomicCAS(status, 0, err);
+}
+
+__global__ void __launch_bounds__(128) overlay_rows_kernel(bf16* __restrict__ hidden, int width,
+                                                           const int32_t* __restrict__ rows,
+                                                           const uint8_t* __restrict__ type,
+                                                           const int32_t* __restrict__ src,
+                                                           const bf16* __restrict__ embeds,
+                                                           const bf16* __restrict__ sentinel,
+                                                           const int* __restrict__ status) {
+  if (*status != 0) return;
+  const int64_t i = blockIdx.x;
+  const int t = type[i];
+  // Sentinel rows in the order START, NEWLINE, END.
+  const bf16* from = t == DS_VIT_TOK_IMAGE ? embeds + static_cast<int64_t>(src[i]) * width
+                     : sentinel + static_cast<int64_t>(t == DS_VIT_TOK_START ? 0 : t == DS_VIT_TOK_NEWLINE ? 1 : 2) * width;
+  const uint4* s4 = reinterpret_cast<const uint4*>(from);
+  uint4* d4 = reinterpret_cast<uint4*>(hidden + static_cast<int64_t>(rows[i]) * width);
+  for (int k = threadIdx.x; k < width / 8; k += blockDim.x) d4[k] = s4[k];
+}
+
 }  // namespace
 
 int launch_layernorm(const bf16* x, const bf16* g, const bf16* b, bf16* y, int64_t M, float eps,
@@ -320,6 +358,18 @@ int launch_overlay(bf16* hidden, int width, const OverlaySpans& spans, const bf1
   const int64_t rows = spans.row_start[spans.n];
   if (rows <= 0) return DS_VIT_OK;
   overlay_kernel<<<static_cast<unsigned>(rows), 128, 0, stream>>>(hidden, width, spans, embeds, sentinel);
+  return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
+}
+
+int launch_overlay_rows(bf16* hidden, int64_t n_hidden, int width, const int32_t* rows, const uint8_t* type,
+                        const int32_t* src, int64_t n, const bf16* embeds, int64_t n_embeds, const bf16* sentinel,
+                        int* status, cudaStream_t stream) {
+  if (n <= 0) return DS_VIT_OK;
+  overlay_rows_check_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, stream>>>(rows, type, src, n, n_hidden,
+                                                                                       n_embeds, status);
+  if (cudaGetLastError() != cudaSuccess) return DS_VIT_ECUDA;
+  overlay_rows_kernel<<<static_cast<unsigned>(n), 128, 0, stream>>>(hidden, width, rows, type, src, embeds, sentinel,
+                                                                    status);
   return cudaGetLastError() == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
 

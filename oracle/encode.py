@@ -45,35 +45,53 @@ F32 = np.float32
 TOK_START, TOK_IMAGE, TOK_NEWLINE, TOK_END = 0, 1, 2, 3
 
 
-# Matrix products.  Every product of the encode goes through ``mm``: an fp32
-# matrix product (BLAS sgemm; summation order is the library's).  With
-# ``products("f64")`` each dot product is accumulated in float64 and rounded to
-# fp32 once (the correctly rounded fp32 result in practice).  The two modes are
-# two valid evaluations of the same fp32 definition; tests use their difference
-# to measure how strongly the bf16 boundaries amplify summation-order noise.
-_PRODUCTS = ["f32"]
+# Evaluation modes.  The definition fixes every bf16 rounding point but not
+# the order of the fp32 sums inside a matrix product, so several evaluations
+# are equally valid; tests use the spread between them to bound how strongly
+# the bf16 boundaries amplify summation-order noise over many layers.
+#
+# ``order`` selects how ``mm`` accumulates each dot product:
+#   "f32"      fp32 matrix product (BLAS sgemm; the library's summation order);
+#   "f64"      accumulated in float64 and rounded to fp32 once (correctly
+#              rounded in practice);
+#   "f32_rev"  fp32 product with the summation index reversed (BLAS again, so
+#              its blocking falls on other terms).
+# ``p_bf16`` selects the attention reading in which the unnormalised softmax
+# numerators exp(s - max) are rounded to bf16 before the product with V and
+# the row sum is taken over the fp32 numerators (a tensor-core kernel feeds P
+# to the PV product as bf16); the default keeps P in fp32.
+_MODE = {"order": "f32", "p_bf16": False}
 
 
 def mm(a, b) -> np.ndarray:
-    if _PRODUCTS[0] == "f64":
+    order = _MODE["order"]
+    if order == "f64":
         return (np.asarray(a, np.float64) @ np.asarray(b, np.float64)).astype(F32)
+    if order == "f32_rev":
+        return (np.ascontiguousarray(np.asarray(a, F32)[:, ::-1])
+                @ np.ascontiguousarray(np.asarray(b, F32)[::-1]))
     return np.asarray(a, F32) @ np.asarray(b, F32)
 
 
-class products:
-    """Context manager selecting the accumulation of ``mm``: "f32" or "f64"."""
+class evaluation:
+    """Context manager selecting the evaluation mode (see above)."""
 
-    def __init__(self, mode: str):
-        assert mode in ("f32", "f64")
-        self.mode = mode
+    def __init__(self, order: str = "f32", p_bf16: bool = False):
+        assert order in ("f32", "f64", "f32_rev")
+        self.mode = {"order": order, "p_bf16": bool(p_bf16)}
 
     def __enter__(self):
-        self.prev = _PRODUCTS[0]
-        _PRODUCTS[0] = self.mode
+        self.prev = dict(_MODE)
+        _MODE.update(self.mode)
         return self
 
     def __exit__(self, *exc):
-        _PRODUCTS[0] = self.prev
+        _MODE.update(self.prev)
+
+
+def products(order: str):
+    """Only the accumulation order of ``mm`` ("f32", "f64" or "f32_rev")."""
+    return evaluation(order, _MODE["p_bf16"])
 
 
 def round_bf16(x) -> np.ndarray:
@@ -260,8 +278,12 @@ def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, heads: int,
     for h in range(heads):
         sl = slice(h * head_dim, (h + 1) * head_dim)
         s = mm(q[:, sl], k[:, sl].T) * scale
-        p = softmax_rows(s)
-        out[:, sl] = mm(p, v[:, sl])
+        if _MODE["p_bf16"]:
+            e = np.exp(s - s.max(axis=-1, keepdims=True))
+            out[:, sl] = mm(round_bf16(e), v[:, sl]) / e.sum(axis=-1, keepdims=True, dtype=F32)
+        else:
+            p = softmax_rows(s)
+            out[:, sl] = mm(p, v[:, sl])
     return round_bf16(out)
 
 
@@ -446,6 +468,21 @@ def overlay_chunk(chunk: np.ndarray, chunk_begin: int, spans, embeds, sentinel):
                     out[i] = sentinel[{TOK_START: 0, TOK_NEWLINE: 1, TOK_END: 2}[int(t)]]
                 row_type[i] = 1 + int(t)
     return out, row_type
+
+
+def overlay_rows(hidden: np.ndarray, rows, types, src, embeds, sentinel) -> np.ndarray:
+    """Copy of ``hidden`` with entry i written at row rows[i]: IMAGE entries take
+    aligner row embeds[src[i]], START / NEWLINE / END entries the learned
+    vector sentinel[0 / 1 / 2] (page A, "Connect the complete image-to-text path
+    first"; the rows may lie anywhere in the prompt).  Entries are applied in
+    order; bit patterns, exact copy."""
+    out = np.array(hidden, copy=True)
+    for r, t, s in zip(rows, types, src):
+        if t == TOK_IMAGE:
+            out[r] = embeds[s]
+        else:
+            out[r] = sentinel[{TOK_START: 0, TOK_NEWLINE: 1, TOK_END: 2}[int(t)]]
+    return out
 
 
 def overlay(hidden: np.ndarray, base_row: int, types, src, embeds, sentinel) -> np.ndarray:

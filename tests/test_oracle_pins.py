@@ -265,6 +265,53 @@ def test_attention_peaked_softmax():
     assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-5)
 
 
+def test_attention_bf16_numerators_reading():
+    """The p_bf16 evaluation: numerators exp(s - max) rounded to bf16 before the
+    product with V, row sums over the unrounded numerators.  Float64 brute force
+    of that reading, and it differs from the fp32-P default by at most the bf16
+    rounding of P."""
+    rng = np.random.default_rng(21)
+    q, k, v = (O.round_bf16(rng.standard_normal((7, 128)).astype(F32) * sc) for sc in (3, 3, 1))
+    with O.evaluation("f32", p_bf16=True):
+        got = O.attention(q, k, v, heads=2)
+    ref, mag = np.zeros((7, 128)), np.zeros((7, 128))
+    for h in range(2):
+        sl = slice(64 * h, 64 * h + 64)
+        s = q[:, sl].astype(np.float64) @ k[:, sl].astype(np.float64).T / 8.0
+        e = np.exp(s - s.max(axis=1, keepdims=True))
+        ref[:, sl] = _bf16(e) @ v[:, sl] / e.sum(axis=1, keepdims=True)
+        mag[:, sl] = e @ np.abs(v[:, sl]) / e.sum(axis=1, keepdims=True)    # sum of p |v|
+    # each side rounds its output to bf16 once (2^-9 relative) after fp32 sums
+    assert np.all(np.abs(got - ref) <= 2 ** -8 * np.abs(ref) + 1e-5 * mag)
+    base = O.attention(q, k, v, heads=2)
+    assert not np.array_equal(got, base)                  # the reading changes results
+    # P's own rounding moves the output by at most 2^-9 of sum p |v| (plus 2^-9
+    # of it again through the row sum), besides the two output roundings
+    assert np.all(np.abs(got - base) <= 2 ** -8 * mag + 2 ** -8 * np.abs(base) + 1e-6)
+
+
+def test_product_orders_are_valid_evaluations():
+    """Every accumulation order of ``mm`` is the same product within the fp32
+    bound K * 2^-24 * (|a| |b|); the reversed order is a different evaluation."""
+    rng = np.random.default_rng(22)
+    a = rng.standard_normal((16, 1024)).astype(F32)
+    b = rng.standard_normal((1024, 24)).astype(F32)
+    exact = a.astype(np.float64) @ b.astype(np.float64)
+    bound = 1024 * 2.0 ** -24 * (np.abs(a).astype(np.float64) @ np.abs(b).astype(np.float64))
+    outs = {}
+    for order in ("f32", "f64", "f32_rev"):
+        with O.evaluation(order):
+            outs[order] = O.mm(a, b)
+        assert outs[order].dtype == F32
+        assert np.all(np.abs(outs[order] - exact) <= bound)
+    assert np.abs(outs["f64"] - exact).max() <= 2.0 ** -23 * np.abs(exact).max()
+    assert not np.array_equal(outs["f32_rev"], outs["f32"])
+    with O.evaluation("f64", True):
+        with O.products("f32_rev"):                       # keeps the P reading
+            assert O.encode.__module__ == "oracle.encode"
+    assert O.mm(a, b).dtype == F32                        # modes restored on exit
+
+
 def test_softmax_rows_sum_to_one():
     s = np.random.default_rng(12).standard_normal((50, 300)).astype(F32) * 20
     p = O.softmax_rows(s)
@@ -485,6 +532,26 @@ def test_overlay_exact_and_untouched():
     assert np.array_equal(out[10], sent[0]) and np.array_equal(out[10 + n - 1], sent[2])
     assert np.array_equal(out[11:14], emb[0:3]) and np.array_equal(out[14], sent[1])
     assert np.array_equal(out[15:18], emb[3:6]) and np.array_equal(out[18], sent[1])
+
+
+def test_overlay_rows_contiguous_equals_span_and_scattered_rows():
+    """With rows = base + r the per-row form is the span overlay; scattered
+    rows (text rows interleaved) write each listed row from its own source and
+    leave every other row untouched."""
+    rng = np.random.default_rng(24)
+    hidden = rng.integers(0, 65535, size=(64, 32), dtype=np.uint16)
+    emb = rng.integers(0, 65535, size=(6, 32), dtype=np.uint16)
+    sent = rng.integers(0, 65535, size=(3, 32), dtype=np.uint16)
+    ids, pos, typ, src = O.layout(6, 9, 1, base_pos=10)
+    assert np.array_equal(O.overlay_rows(hidden, pos, typ, src, emb, sent),
+                          O.overlay(hidden, 10, typ, src, emb, sent))
+    rows = np.sort(rng.choice(64, len(typ), replace=False))
+    out = O.overlay_rows(hidden, rows, typ, src, emb, sent)
+    for r, t, s_ in zip(rows, typ, src):
+        want = emb[s_] if t == O.TOK_IMAGE else sent[{0: 0, 2: 1, 3: 2}[int(t)]]
+        assert np.array_equal(out[r], want)
+    rest = np.setdiff1d(np.arange(64), rows)
+    assert np.array_equal(out[rest], hidden[rest])
 
 
 def _two_span_prompt(rng, rows=120, width=16):

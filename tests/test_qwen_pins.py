@@ -107,6 +107,91 @@ def test_block_identity_with_zero_branches():
     assert np.array_equal(Q.block(x, L, Q.QWEN, gy, gx), x)
 
 
+def _small_qwen_layer(seed, D=144, F=288):
+    rng = np.random.default_rng(seed)
+    n = lambda *sh: WL.to_bf16_bits(rng.standard_normal(sh).astype(F32) * 0.1)
+    g = lambda: WL.to_bf16_bits(1 + rng.standard_normal(D).astype(F32) * 0.1)
+    return dict(ln1_g=g(), ln1_b=n(D), qkv_w=n(3 * D, D), qkv_b=n(3 * D), proj_w=n(D, D), proj_b=n(D),
+                ln2_g=g(), ln2_b=n(D), fc1_w=n(F, D), fc1_b=n(F), fc2_w=n(D, F), fc2_b=n(D))
+
+
+def _bf16(a):
+    """Round to bf16 through torch (an independent RNE routine), back to float64."""
+    import torch
+    return torch.from_numpy(np.asarray(a, np.float64)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _qwen_block_bruteforce(x, L, gy, gx, heads=2, hd=72, theta=10000.0, eps=1e-6):
+    """The Qwen-style block in float64 loops, each step from its definition,
+    with the stored activations rounded to bf16 where the oracle's header puts
+    them: LN outputs, the QKV projection before the rotation, q and k after it,
+    the attention output, the residual stream and the MLP hidden."""
+    f = {k: O.bits_to_f32(v).astype(np.float64) for k, v in L.items()}
+    n, D = x.shape
+
+    def ln(a, g, b):
+        out = np.zeros_like(a)
+        for i in range(n):
+            mu = sum(a[i]) / D
+            var = sum((t - mu) ** 2 for t in a[i]) / D
+            out[i] = [(a[i, j] - mu) / math.sqrt(var + eps) * g[j] + b[j] for j in range(D)]
+        return out
+
+    def lin(a, w, b):
+        return np.array([[sum(a[i, t] * w[o, t] for t in range(a.shape[1])) + b[o]
+                          for o in range(w.shape[0])] for i in range(a.shape[0])])
+
+    fr = [theta ** (-j / 18) for j in range(18)]
+
+    def rot(vec, i):
+        out = vec.copy()
+        for h in range(heads):
+            for half, pos in ((0, gy[i]), (1, gx[i])):
+                base = h * hd + half * 36
+                for j in range(18):
+                    c, s = math.cos(pos * fr[j]), math.sin(pos * fr[j])
+                    a, b = vec[base + j], vec[base + j + 18]
+                    out[base + j], out[base + j + 18] = a * c - b * s, b * c + a * s
+        return out
+
+    x = x.astype(np.float64)
+    y = _bf16(ln(x, f["ln1_g"], f["ln1_b"]))
+    t = _bf16(lin(y, f["qkv_w"], f["qkv_b"]))
+    q = _bf16([rot(t[i, :D], i) for i in range(n)])
+    k = _bf16([rot(t[i, D:2 * D], i) for i in range(n)])
+    v = t[:, 2 * D:]
+    o = np.zeros((n, D))
+    for h in range(heads):
+        sl = slice(h * hd, (h + 1) * hd)
+        for i in range(n):
+            sc = [sum(q[i, sl] * k[j, sl]) / math.sqrt(hd) for j in range(n)]
+            m = max(sc)
+            e = [math.exp(a - m) for a in sc]
+            o[i, sl] = sum(e[j] * v[j, sl] for j in range(n)) / sum(e)
+    o = _bf16(o)
+    x = _bf16(x + lin(o, f["proj_w"], f["proj_b"]))
+    y = _bf16(ln(x, f["ln2_g"], f["ln2_b"]))
+    hdn = lin(y, f["fc1_w"], f["fc1_b"])
+    g = _bf16([[0.5 * a * (1 + math.erf(a / math.sqrt(2))) for a in row] for row in hdn])
+    return _bf16(x + lin(g, f["fc2_w"], f["fc2_b"]))
+
+
+def test_block_against_float64_bruteforce():
+    """Q.block at hidden 144 (2 heads of 72) on a 2 x 4 grid in merge-group
+    order, against the float64 brute force; a transposed projection, a wrong
+    head split (4 heads of 36) and swapped RoPE axes are each far off."""
+    cfg = dict(Q.QWEN, hidden=144, heads=2, mlp=288)
+    L = _small_qwen_layer(67)
+    x = O.round_bf16(np.random.default_rng(68).standard_normal((8, 144)).astype(F32))
+    gy, gx = Q.patch_order(2, 4)
+    ref = _qwen_block_bruteforce(x, L, gy, gx)
+    err = lambda got: (np.abs(got - ref) / (1 + np.abs(ref))).max()
+    assert err(Q.block(x, L, cfg, gy, gx)) < 2 ** -7           # allows a rare one-ulp rounding flip
+    assert err(Q.block(x, dict(L, proj_w=np.ascontiguousarray(L["proj_w"].T)), cfg, gy, gx)) > 0.05
+    assert err(Q.block(x, L, dict(cfg, heads=4, head_dim=36), gy, gx)) > 0.05
+    assert err(Q.block(x, L, cfg, gx, gy)) > 0.05
+
+
 def test_merger_concatenates_each_group_in_order():
     """One-hot w1 rows pick column r*1152 + c of the group concatenation: the
     c-th channel of the group's r-th patch (after the merger LayerNorm)."""

@@ -56,6 +56,18 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, source="fallback")
 
 
+def tensor_peak(pk, clk):
+    """The measured bf16 peak that applies to a kernel timed at the sampled SM
+    clock: the burst figure (cuBLAS timed alone, at the maximum SM clock) when
+    the median SM clock under load is within 5% of the maximum, else the
+    sustained one (a seconds-long loop under the power cap, at a lower clock).
+    Returns (peak TFLOP/s, label)."""
+    if clk and clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"]:
+        return pk["bf16_sus"], f"{pk['source']} bf16 dense, sustained (median SM clock {clk['sm_mhz']:.0f} MHz)"
+    mhz = f"{clk['sm_mhz']:.0f} MHz" if clk and clk.get("sm_mhz") else "not sampled"
+    return pk["bf16"], f"{pk['source']} bf16 dense, burst (median SM clock {mhz}, at its maximum)"
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -144,31 +156,81 @@ def _threads():
     return int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count())))
 
 
+def _oracle_block_timing(imgs, n_layers, cfg, W):
+    """Oracle time of one encode of ``imgs``: patch projection, block 0 over
+    all packed patches (measured), final LN + merger (measured); the whole
+    encode derived as embed + n_layers x block + merger.  Returns
+    (embed_s, block_s, merger_s, tokens)."""
+    import numpy as np
+
+    import oracle as O
+    grids = [(im.shape[0] // 14, im.shape[1] // 14) for im in imgs]
+    t0 = time.perf_counter()
+    P = np.concatenate([O.normalise(O.patchify(im), cfg["mean"], cfg["std"]) for im in imgs])
+    x = O.round_bf16(O.mm(P, O.bits_to_f32(W["patch_w"]).T) + O.bits_to_f32(W["patch_b"]))
+    t1 = time.perf_counter()
+    gy = np.concatenate([O.grid_positions(*g)[0] for g in grids])
+    gx = np.concatenate([O.grid_positions(*g)[1] for g in grids])
+    seqlens = [gh * gw for gh, gw in grids]
+    x = O.vit_block(x, W["layers"][0], cfg, seqlens, gy, gx)
+    t2 = time.perf_counter()
+    z = O.round_bf16(O.norm(x, W["lnm_g"], W["lnm_b"], cfg))
+    starts = np.concatenate([[0], np.cumsum(seqlens)])
+    A = np.concatenate([O.merge_unfold(z[starts[i]:starts[i + 1]], *grids[i]) for i in range(len(imgs))])
+    O.merger(A, W)
+    t3 = time.perf_counter()
+    return t1 - t0, t2 - t1, t3 - t2, A.shape[0]
+
+
 def cpu_baseline():
     """The oracle as it stands, on a bounded sample of the same workload: the
     1344x1344 image through patch projection, one ViT block over all 9216
-    patches, the final LN and the merger.  Full-encode time is estimated as
-    embed + 32 x block + merger."""
-    import oracle as O
+    patches, the final LN and the merger (measured).  The full-encode time is
+    derived as embed + 32 x block + merger."""
     import workloads as WL
     W = WL.make_weights(1)
     img = WL.workload_images(WORKLOAD)[0]
+    emb, blk, mrg, T = _oracle_block_timing([img], N_LAYERS, WL.MODEL, W)
+    full = emb + N_LAYERS * blk + mrg
+    return dict(value=T / full, unit="tokens/s", cores=_threads(), kind="oracle", derived=True,
+                measured={"embed_s": round(emb, 3), "block_s": round(blk, 3), "merger_s": round(mrg, 3)},
+                sample=f"1344x1344 image: patch projection, 1 of the 32 ViT blocks over all 9216 patches, "
+                       f"final LN + merger, measured; full encode derived as embed + 32 x block + merger "
+                       f"= {full:.1f} s (block {blk:.2f} s)")
+
+
+def oracle_timings():
+    """The oracle on every synthetic workload, on the host cores: the tiny
+    image and the 546x546 image as whole encodes (measured); the 2688x336 image
+    and the first five images of the 16-image batch (one cycle of its sizes, a
+    declared subset) as patch projection + one block + merger, measured, with
+    the whole encode derived as embed + 32 x block + merger."""
+    import oracle as O
+    import workloads as WL
     cfg = WL.MODEL
-    t0 = time.perf_counter()
-    P = O.normalise(O.patchify(img), cfg["mean"], cfg["std"])
-    x = O.round_bf16(O.mm(P, O.bits_to_f32(W["patch_w"]).T) + O.bits_to_f32(W["patch_b"]))
-    t1 = time.perf_counter()
-    gy, gx = O.grid_positions(GH, GW)
-    x = O.vit_block(x, W["layers"][0], cfg, [N_PATCH], gy, gx)
-    t2 = time.perf_counter()
-    z = O.round_bf16(O.layer_norm(x, O.bits_to_f32(W["lnm_g"]), O.bits_to_f32(W["lnm_b"]), cfg["ln_eps"]))
-    O.merger(O.merge_unfold(z, GH, GW), W)
-    t3 = time.perf_counter()
-    full = (t1 - t0) + N_LAYERS * (t2 - t1) + (t3 - t2)
-    return dict(value=N_TOK / full, unit="tokens/s", cores=_threads(), kind="oracle",
-                sample=f"1344x1344 image: patch projection, 1 of the 32 ViT blocks over all 9216 "
-                       f"patches, final LN + merger; full encode estimated as embed + 32 x block + "
-                       f"merger = {full:.1f} s (block {t2 - t1:.2f} s)")
+    res = {}
+    for name in ("tiny", "min"):
+        wl = WL.WORKLOADS[name]
+        imgs = WL.workload_images(name)
+        W = WL.make_weights(wl["n_layers"])
+        t0 = time.perf_counter()
+        e, _ = O.encode(imgs, W, cfg)
+        sec = time.perf_counter() - t0
+        res[name] = {"oracle_s": round(sec, 3), "oracle_tokens_per_s": round(e.shape[0] / sec, 3),
+                     "oracle_images_per_s": round(len(imgs) / sec, 4), "cores": _threads(), "derived": False,
+                     "sample": "whole encode"}
+    W1 = WL.make_weights(1)
+    for name, imgs, label in (("aspect", WL.workload_images("aspect")[:1], "one 2688x336 image"),
+                              ("batch16", WL.workload_images("batch16")[:5],
+                               "subset: the first 5 of the 16 images (one cycle of the sizes)")):
+        emb, blk, mrg, T = _oracle_block_timing(imgs, N_LAYERS, cfg, W1)
+        full = emb + N_LAYERS * blk + mrg
+        res[name] = {"oracle_s": round(full, 2), "oracle_tokens_per_s": round(T / full, 3),
+                     "oracle_images_per_s": round(len(imgs) / full, 5), "cores": _threads(), "derived": True,
+                     "measured": {"embed_s": round(emb, 3), "block_s": round(blk, 3), "merger_s": round(mrg, 3)},
+                     "sample": f"{label}: patch projection, 1 of the 32 blocks, final LN + merger measured; "
+                               f"whole encode derived as embed + 32 x block + merger"}
+    return res
 
 
 def run_reference(args):
@@ -202,16 +264,20 @@ def run_reference(args):
     full = t_embed + N_LAYERS * block + t_merge
     value = N_TOK / full
     sample = (f"each step: one of the 32 ViT blocks of the oracle over all 9216 patches of the 1344x1344 "
-              f"image; full encode estimated as embed ({t_embed:.2f} s) + 32 x mean block ({block:.2f} s) "
-              f"+ final LN and merger ({t_merge:.2f} s)")
+              f"image (measured, {block:.2f} s mean); the value is derived for the whole encode as embed "
+              f"({t_embed:.2f} s) + 32 x mean block + final LN and merger ({t_merge:.2f} s) = {full:.1f} s")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full * 1e3, "higher_is_better": True,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": block * 1e3,
+        "step": "one ViT block of the oracle (measured); value derived for the whole encode",
+        "derived_encode_s": full, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": "1344x1344 uint8 uniform (seed 3), 9216 patches, 32 layers, 1024 tokens; "
                                "CPU oracle (numpy fp32 with bf16 rounding)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": _threads(), "kind": "oracle",
-                         "sample": sample},
+                         "derived": True, "sample": sample,
+                         "measured": {"embed_s": round(t_embed, 3), "block_s": round(block, 3),
+                                      "merger_s": round(t_merge, 3)}},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 
@@ -261,7 +327,7 @@ def qwen_workload(pk, reps: int = 5, H: int = 1024, W: int = 1024):
     return {"tower": "Qwen3-VL-style: 16x16x2 patches, 27 blocks of 1152 (16 heads of 72), 2x2 merger + 3 DeepStack",
             "image": [H, W], "patches": N, "tokens": T, "ms_per_encode": round(sec * 1e3, 4),
             "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
-            "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3),
+            "frac_of_peak": round(fl / sec / 1e12 / pk["tc"], 3),
             "note": "heads padded to 80 in the QKV projection and attention tiles; FLOPs counted at 72"}
 
 
@@ -294,7 +360,7 @@ def official_workload(pk, reps: int = 5):
     return {"variant": "RMSNorm, SwiGLU (4096 gate + 4096 up), half-vector RoPE pairing, [-1, 1] pixels",
             "image": [int(img.shape[0]), int(img.shape[1])], "layers": N_LAYERS, "tokens": N_TOK,
             "ms_per_encode": round(sec * 1e3, 4), "tokens_per_s": round(N_TOK / sec, 1),
-            "tflops": round(fl / sec / 1e12, 1), "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3)}
+            "tflops": round(fl / sec / 1e12, 1), "frac_of_peak": round(fl / sec / 1e12 / pk["tc"], 3)}
 
 
 def other_workloads(dw, cfg, pk, reps: int = 5):
@@ -329,7 +395,7 @@ def other_workloads(dw, cfg, pk, reps: int = 5):
         res[name] = {"images": len(imgs), "layers": wl["n_layers"], "tokens": T,
                      "ms_per_encode": round(sec * 1e3, 4), "images_per_s": round(len(imgs) / sec, 2),
                      "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
-                     "frac_of_peak": round(fl / sec / 1e12 / pk["bf16_sus"], 3)}
+                     "frac_of_peak": round(fl / sec / 1e12 / pk["tc"], 3)}
         if enc.status() != dv.OK:
             raise RuntimeError(f"device status after {name}")
         enc.close()
@@ -600,6 +666,7 @@ def main():
     _, e2e_value = aggregate(e0.elapsed_time(e1) / 1e3, N_TOK * args.steps, world)
 
     pk = peaks()
+    pk["tc"], pk["tc_label"] = tensor_peak(pk, clk)
     attn_ms, attn_n = per_kind["attention"]
     attn_tflops = KIND_FLOP["attention"] / (attn_ms / attn_n / 1e3) / 1e12
     kernels = {}
@@ -607,7 +674,7 @@ def main():
         d = {"launches_per_step": n / args.steps, "ms_per_step": round(ms / args.steps, 4)}
         if k in KIND_FLOP:
             d["tflops"] = round(KIND_FLOP[k] * n / (ms / 1e3) / 1e12, 1)
-            d["frac_of_peak"] = round(d["tflops"] / pk["bf16_sus"], 3)
+            d["frac_of_peak"] = round(d["tflops"] / pk["tc"], 3)
         kernels[k] = d
     ms_step = tmax / args.steps * 1e3
     line = {
@@ -623,10 +690,11 @@ def main():
                    "weights": "random N(0,0.02), seed 1000"},
         "images_per_s": value / N_TOK,
         "encode_tflops": ENCODE_FLOP / (ms_step / 1e3) / 1e12,
-        "encode_tc_peak_frac": ENCODE_FLOP / (ms_step / 1e3) / 1e12 / pk["bf16_sus"],
+        "encode_tc_peak_frac": ENCODE_FLOP / (ms_step / 1e3) / 1e12 / pk["tc"],
         "roofline": {"bound": "tensor", "kernel": "attention", "achieved": attn_tflops,
-                     "peak": pk["bf16_sus"], "unit": "TFLOP/s", "frac": attn_tflops / pk["bf16_sus"],
-                     "peak_kind": f"{pk['source']} bf16 dense, sustained (kernel timed inside a long step)",
+                     "peak": pk["tc"], "unit": "TFLOP/s", "frac": attn_tflops / pk["tc"],
+                     "peak_kind": pk["tc_label"],
+                     "frac_of_burst": attn_tflops / pk["bf16"], "frac_of_sustained": attn_tflops / pk["bf16_sus"],
                      "flop_per_launch": KIND_FLOP["attention"], "traffic": measured_traffic()},
         "kernels": kernels,
         "gpu_launches": gpu_launches,
@@ -643,6 +711,9 @@ def main():
         line["qwen_tower"] = qwen_workload(pk)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+        if "workloads" in line:
+            for name, d in oracle_timings().items():
+                line["workloads"][name]["oracle"] = d
     if rank == 0:
         print(json.dumps(line), flush=True)
     enc.close()

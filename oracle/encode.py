@@ -56,11 +56,27 @@ TOK_START, TOK_IMAGE, TOK_NEWLINE, TOK_END = 0, 1, 2, 3
 #              rounded in practice);
 #   "f32_rev"  fp32 product with the summation index reversed (BLAS again, so
 #              its blocking falls on other terms).
+# The order also governs the row statistics of the norms (mean and variance,
+# or mean square): numpy's fp32 pairwise sum, a float64 sum, or the fp32 sum
+# over the reversed row.
 # ``p_bf16`` selects the attention reading in which the unnormalised softmax
 # numerators exp(s - max) are rounded to bf16 before the product with V and
 # the row sum is taken over the fp32 numerators (a tensor-core kernel feeds P
 # to the PV product as bf16); the default keeps P in fp32.
-_MODE = {"order": "f32", "p_bf16": False}
+# ``fn32`` evaluates GELU and SiLU in fp32 arithmetic (fp32 erf / exp and fp32
+# products) instead of float64 cast to fp32: the same functions, rounded
+# differently.
+_MODE = {"order": "f32", "p_bf16": False, "fn32": False}
+
+
+def _row_mean(x: np.ndarray) -> np.ndarray:
+    """Mean over the last axis in the order of the evaluation mode, as fp32."""
+    order = _MODE["order"]
+    if order == "f64":
+        return x.astype(np.float64).mean(axis=-1, keepdims=True).astype(F32)
+    if order == "f32_rev":
+        return x[..., ::-1].mean(axis=-1, dtype=F32, keepdims=True)
+    return x.mean(axis=-1, dtype=F32, keepdims=True)
 
 
 def mm(a, b) -> np.ndarray:
@@ -76,9 +92,9 @@ def mm(a, b) -> np.ndarray:
 class evaluation:
     """Context manager selecting the evaluation mode (see above)."""
 
-    def __init__(self, order: str = "f32", p_bf16: bool = False):
+    def __init__(self, order: str = "f32", p_bf16: bool = False, fn32: bool = False):
         assert order in ("f32", "f64", "f32_rev")
-        self.mode = {"order": order, "p_bf16": bool(p_bf16)}
+        self.mode = {"order": order, "p_bf16": bool(p_bf16), "fn32": bool(fn32)}
 
     def __enter__(self):
         self.prev = dict(_MODE)
@@ -90,8 +106,8 @@ class evaluation:
 
 
 def products(order: str):
-    """Only the accumulation order of ``mm`` ("f32", "f64" or "f32_rev")."""
-    return evaluation(order, _MODE["p_bf16"])
+    """Only the accumulation order ("f32", "f64" or "f32_rev")."""
+    return evaluation(order, _MODE["p_bf16"], _MODE["fn32"])
 
 
 def round_bf16(x) -> np.ndarray:
@@ -220,9 +236,9 @@ def rope(v: np.ndarray, gy: np.ndarray, gx: np.ndarray, theta: float) -> np.ndar
 def layer_norm(x: np.ndarray, g: np.ndarray, b: np.ndarray, eps: float) -> np.ndarray:
     """(x - mu) * (1/sqrt(var + eps)) * g + b over the last axis, fp32, biased variance."""
     x = x.astype(F32)
-    mu = x.mean(axis=-1, dtype=F32, keepdims=True)
+    mu = _row_mean(x)
     d = x - mu
-    var = (d * d).mean(axis=-1, dtype=F32, keepdims=True)
+    var = _row_mean(d * d)
     inv = F32(1.0) / np.sqrt(var + F32(eps))
     return d * inv * g.astype(F32) + b.astype(F32)
 
@@ -232,7 +248,7 @@ def rms_norm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
     comparison table: the official vision tower uses RMSNorm; "Step 2" table:
     "RMSNorm semantics" at the final norm output)."""
     x = x.astype(F32)
-    ms = (x * x).mean(axis=-1, dtype=F32, keepdims=True)
+    ms = _row_mean(x * x)
     inv = F32(1.0) / np.sqrt(ms + F32(eps))
     return x * inv * g.astype(F32)
 
@@ -245,7 +261,11 @@ def norm(x: np.ndarray, g, b, cfg: dict) -> np.ndarray:
 
 
 def silu(z: np.ndarray) -> np.ndarray:
-    """z * sigmoid(z) = z / (1 + exp(-z)), float64, returned as fp32."""
+    """z * sigmoid(z) = z / (1 + exp(-z)), float64, returned as fp32 (fp32
+    arithmetic under the fn32 evaluation mode)."""
+    if _MODE["fn32"]:
+        zf = np.asarray(z, dtype=F32)
+        return zf / (F32(1.0) + np.exp(-zf))
     zz = np.asarray(z, dtype=np.float64)
     return (zz / (1.0 + np.exp(-zz))).astype(F32)
 
@@ -253,7 +273,12 @@ def silu(z: np.ndarray) -> np.ndarray:
 def gelu(z: np.ndarray) -> np.ndarray:
     """GELU with erf (page A, "End-to-end results and their limits": the official
     vision path uses erf, not the tanh approximation): 0.5 z (1 + erf(z/sqrt 2)),
-    evaluated in float64, returned as fp32."""
+    evaluated in float64, returned as fp32 (fp32 arithmetic under the fn32
+    evaluation mode)."""
+    if _MODE["fn32"]:
+        zf = np.asarray(z, dtype=F32)
+        e = _erf(zf * F32(1.0 / math.sqrt(2.0))).astype(F32)
+        return F32(0.5) * zf * (F32(1.0) + e)
     zz = np.asarray(z, dtype=np.float64)
     return (0.5 * zz * (1.0 + _erf(zz / math.sqrt(2.0)))).astype(F32)
 

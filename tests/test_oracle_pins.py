@@ -290,6 +290,33 @@ def test_attention_bf16_numerators_reading():
     assert np.all(np.abs(got - base) <= 2 ** -8 * mag + 2 ** -8 * np.abs(base) + 1e-6)
 
 
+def test_fp32_function_mode_and_norm_orders():
+    """fn32 evaluates GELU / SiLU in fp32 arithmetic: within a few fp32 units
+    of the float64 closed form (and not always equal to the float64 path);
+    every norm-statistics order gives the same LayerNorm / RMSNorm within fp32
+    rounding (and the float64 order differs from the default somewhere)."""
+    z = np.linspace(-8, 8, 20001, dtype=F32)
+    ref = 0.5 * z.astype(np.float64) * (1 + np.array([math.erf(v / math.sqrt(2)) for v in z.astype(np.float64)]))
+    with O.evaluation("f32", fn32=True):
+        g32 = O.gelu(z)
+        s32 = O.silu(z)
+    assert g32.dtype == F32 and s32.dtype == F32
+    assert np.all(np.abs(g32 - ref) <= 4 * 2.0 ** -24 * (np.abs(ref) + 1.0))
+    assert not np.array_equal(g32, O.gelu(z))
+    sref = z.astype(np.float64) / (1 + np.exp(-z.astype(np.float64)))
+    assert np.all(np.abs(s32 - sref) <= 4 * 2.0 ** -24 * (np.abs(sref) + 1.0))
+    x = np.random.default_rng(25).standard_normal((64, 1024)).astype(F32) * 3 + 1
+    g, b = np.full(1024, 1.0, F32), np.zeros(1024, F32)
+    base, rbase = O.layer_norm(x, g, b, 1e-6), O.rms_norm(x, g, 1e-6)
+    outs = []
+    for order in ("f64", "f32_rev"):
+        with O.evaluation(order):
+            outs.append(O.layer_norm(x, g, b, 1e-6))
+            rms = O.rms_norm(x, g, 1e-6)
+        assert np.abs(outs[-1] - base).max() <= 1e-5 and np.abs(rms - rbase).max() <= 1e-5
+    assert not np.array_equal(outs[0], base)
+
+
 def test_product_orders_are_valid_evaluations():
     """Every accumulation order of ``mm`` is the same product within the fp32
     bound K * 2^-24 * (|a| |b|); the reversed order is a different evaluation."""

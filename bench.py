@@ -5,7 +5,7 @@ tokens at width 5120), plus the token layout and the overlay of the span into
 a 4096 x 5120 prompt buffer.  One step = one pass of that whole path.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-  python bench.py --profile encode|attention|gemm-qkv|gemm-fc1|gemm-fc2   (for ncu)
+  python bench.py --profile encode|attention|overlay|gemm-qkv|gemm-fc1|gemm-fc2|gemm-proj   (for ncu)
 
 N > 1 runs under torchrun: every rank encodes its own copy of the workload
 (replicas, no data-path collective); the timed region is bracketed by barriers
@@ -466,22 +466,39 @@ def overlay_chunk_timing(pk, chunk_rows: int = 2048, reps: int = 20):
         for a, b in chunks:
             dv.overlay_chunk(hidden[a:b], a, spans, emb, sent, row_type=mask[a:b])
 
-    for _ in range(3):
-        run()
-    torch.cuda.synchronize()
-    per = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        run()
-        e1.record()
+    def timed(fn):
+        for _ in range(3):
+            fn()
         torch.cuda.synchronize()
-        per.append(e0.elapsed_time(e1) / 1e3)
-    sec = statistics.median(per)
+        per = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / 1e3)
+        return statistics.median(per)
+
+    eager = timed(run)
+    # The same calls captured once in a CUDA graph and replayed (how a prefill
+    # loop that owns a graph would issue them): the launches no longer wait on
+    # the host.
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run()
+    sec = timed(g.replay)
     nbytes = sum(rows) * 5120 * 2 * 2 + 16384
     return {"prompt_rows": 16384, "span_rows": sum(rows), "chunk_rows": chunk_rows, "chunks": len(chunks),
             "ms": round(sec * 1e3, 4), "algorithmic_bytes": nbytes, "gb_per_s": round(nbytes / sec / 1e9, 1),
-            "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm"], 3)}
+            "frac_of_hbm": round(nbytes / sec / 1e9 / pk["hbm"], 3), "timing": "CUDA graph of the chunk calls",
+            "eager_ms": round(eager * 1e3, 4),
+            "eager_frac_of_hbm": round(nbytes / eager / 1e9 / pk["hbm"], 3)}
 
 
 def run_profile_case(case: str):
@@ -501,6 +518,19 @@ def run_profile_case(case: str):
         img = torch.from_numpy(WL.workload_images(WORKLOAD)[0]).cuda()
         out = torch.empty((N_TOK, 5120), dtype=torch.bfloat16, device="cuda")
         run = lambda: enc.encode([img], out=out)
+    elif case == "overlay":
+        # One 1,058-row span into the 4096 x 5120 prompt at the seeded base.
+        hidden = torch.from_numpy(WL.hidden_buffer(4096, 5120, WL.WORKLOADS[WORKLOAD]["hidden_seed"])
+                                  .view(np.int16)).cuda().view(torch.bfloat16)
+        emb = torch.randn((N_TOK, 5120), device="cuda").to(torch.bfloat16)
+        sent = torch.randn((3, 5120), device="cuda").to(torch.bfloat16)
+        n_rows = len(dv.layout(GH, GW, WL.MODEL["image_token_id"])[0])
+        base = WL.span_bases(WORKLOAD, [n_rows])[0]
+        flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+        def run():
+            flush.zero_()                   # evict L2 so the counters see DRAM traffic
+            dv.overlay(hidden, [(base, GH, GW, 0)], emb, sent)
     elif case == "attention":
         qkv = torch.from_numpy(WL.to_bf16_bits(rng.standard_normal((N_PATCH, 3072), dtype=np.float32))
                                .view(np.int16)).cuda().view(torch.bfloat16)

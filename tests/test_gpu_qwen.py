@@ -13,7 +13,8 @@ import pytest
 import oracle as O
 import oracle.qwen as Q
 import workloads as WL
-from gpu_util import COS_MIN, FLOOR_FACTOR, REL_TOL, assert_parity, bits_of, dev, host, rand_bits, rel_err, row_cos
+from gpu_util import (SPREAD_MODES, assert_parity, assert_within_spread, bits_of, dev, host, rand_bits,
+                      rel_err, spread_of)
 
 pytestmark = pytest.mark.gpu
 
@@ -78,17 +79,14 @@ def test_qwen_encode(dv, encq, wq, H, W):
         assert_parity(bits_of(bl[l + 1]), ref, what=f"block {l}")
     assert_parity(host(out), Q.merger(bits_of(bl[N_LAYERS]), wq["merger"], cfg), what="merger")
     assert_parity(host(deep[0]), Q.merger(bits_of(bl[8]), wq["deepstack"][0], cfg), what="deepstack 8")
-    # free-running outputs against the oracle, bounded by its own spread
-    ref_out, ref_deep = Q.encode(img, wq, cfg, n_layers=N_LAYERS)
-    with O.products("f64"):
-        alt_out, alt_deep = Q.encode(img, wq, cfg, n_layers=N_LAYERS)
-    for got, ref, alt, what in ((host(out), ref_out, alt_out, "primary"),
-                                (host(deep[0]), ref_deep[0], alt_deep[0], "deepstack 8")):
-        floor = rel_err(alt, ref)
-        e = rel_err(got, ref)
-        assert row_cos(got, ref).min() >= COS_MIN, what
-        assert e.max() <= max(REL_TOL, FLOOR_FACTOR * floor.max()), (what, e.max(), floor.max())
-        assert e.mean() <= max(REL_TOL / 10, FLOOR_FACTOR * floor.mean()), (what, e.mean())
+    # free-running outputs against the oracle, within the spread of its valid evaluations
+    outs = []
+    for mode in SPREAD_MODES:
+        with O.evaluation(*mode):
+            prim, deep_ref = Q.encode(img, wq, cfg, n_layers=N_LAYERS)
+        outs.append((prim, deep_ref[0]))
+    assert_within_spread(host(out), outs[0][0], spread_of([o[0] for o in outs]), what="primary")
+    assert_within_spread(host(deep[0]), outs[0][1], spread_of([o[1] for o in outs]), what="deepstack 8")
 
 
 def test_qwen_rejects_bad_sizes(dv, encq):

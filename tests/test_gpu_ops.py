@@ -59,7 +59,9 @@ GEMM_CASES = [
     # K = 4096; M = 4200, whose last tile's second 128-row half lies wholly past
     # M; the second merger linear's K = N = 5120.
     (3840, 4096, 1024, "resid"), (4200, 2048, 1024, "gelu"), (4200, 4096, 1024, "resid"),
-    (1024, 5120, 5120, "bias"),
+    # The merger linears' width at about a thousand rows: 320-wide tiles in one
+    # round (two MMAs per K step, a 256-row and a 64-row B box); ragged M.
+    (1024, 5120, 5120, "bias"), (1100, 2048, 5120, "gelu"), (1000, 1024, 5120, "bias"),
 ]
 
 

@@ -26,6 +26,10 @@
 // the main loop of the next.  The tile's bias is staged once in shared memory;
 // each 32x32 output chunk goes through a 64-byte-swizzled shared staging tile
 // (two per warp) and leaves by TMA store, which also clips rows past M.
+// 320-wide tiles (the merger linears, N = 5120, at sizes where 256-wide tiles
+// need a second, almost empty round) issue two MMAs per K step (N = 256 and
+// N = 64 into adjacent TMEM columns), load B as a 256-row and a 64-row box,
+// and keep one accumulator (320 of the 512 columns).
 // Where 256-wide tiles are chosen and A comes by TMA, the 2-CTA-cluster
 // kernel runs instead (gemm_pair.cu, 256 x 256 tiles, same epilogue source);
 // this kernel keeps 128-wide tiles, the produced-A GEMMs and devices where no
@@ -52,7 +56,7 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // The pixel producer's raw-byte ring and LUT take the room of one stage.
-  static constexpr int STAGES = (BN == 256 ? 4 : 6) - (ASRC == kAPixels ? 1 : 0);
+  static constexpr int STAGES = (BN == 320 ? 3 : BN == 256 ? 4 : 6) - (ASRC == kAPixels ? 1 : 0);
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 32 * 2;                // one 32x32 bf16 chunk
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;         // 2 staging chunks per warp
@@ -66,7 +70,8 @@ struct GemmCfg {
   static constexpr int OFF_LUT = OFF_RAW + RAW_SLOTS * BM * RAW_ROW;
   static constexpr int OFF_BAR = ASRC == kAPixels ? OFF_LUT + 3 * 256 * 2 : OFF_RAW;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;      // + barriers + alignment slack
-  static constexpr int TMEM_COLS = 2 * BN;
+  static constexpr int ACCS = 2 * BN <= 512 ? 2 : 1;           // TMEM accumulators
+  static constexpr int TMEM_COLS = ACCS == 2 ? 2 * BN : 512;
   // Warps 0-7 epilogue, 8 TMA, 9 MMA; with a produced A, warps 10-13 build the A
   // tiles (one row per thread) and 14-15 idle: 16 warps keep every SM
   // sub-partition within 4 x 32 x 128 registers.
@@ -76,6 +81,8 @@ static_assert(GemmCfg<256>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<256, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<320>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<320, kAMerge>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(3 * GemmCfg<128>::STAGES + 5 <= 31, "barrier slots");
 
 // Image of packed row `row` (offsets `off`, n images) and the row's index in it.
@@ -269,9 +276,10 @@ __device__ __forceinline__ void produce_a_pixels(const AGenParams& g, const Gemm
 template <int BN, int EPI, int ASRC>
 __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmC, const GemmParams p,
-                const __grid_constant__ AGenParams g) {
+                const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmB64,
+                const GemmParams p, const __grid_constant__ AGenParams g) {
   using C = GemmCfg<BN, ASRC>;
+  constexpr uint32_t kAccs = C::ACCS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -312,6 +320,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     if constexpr (ASRC == kATma) prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmC);
+    if constexpr (BN == 320) prefetch_tensormap(&tmB64);
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -349,6 +358,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
             tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * (BN / 2));
             tma_load_2d(stage_b(stage) + (BN / 2) * C::BK * 2, &tmB, full_bar(stage), kb * C::BK,
                         p.N / 2 + nb * (BN / 2));
+          } else if constexpr (BN == 320) {
+            tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
+            tma_load_2d(stage_b(stage) + 256 * C::BK * 2, &tmB64, full_bar(stage), kb * C::BK, nb * BN + 256);
           } else {
             tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
           }
@@ -364,7 +376,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN, false, false);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN == 320 ? 256 : BN, false, false);
+      constexpr uint32_t idesc64 = idesc_bf16_f32(128, 64, false, false);
       // Descriptors are built once; a stage or K step only advances the start
       // address field (byte offset >> 4).
       const uint64_t da0 = sdesc_sw128(stage_a(0), 16, 1024);
@@ -391,8 +404,13 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
           tc_fence_after();
           const uint64_t off = static_cast<uint64_t>(stage * (C::STAGE_BYTES >> 4));
 #pragma unroll
-          for (int k = 0; k < C::BK / 16; ++k)
+          for (int k = 0; k < C::BK / 16; ++k) {
             umma_bf16(d_tmem, da0 + off + 2 * k, db0 + off + 2 * k, idesc, (kb | k) != 0);
+            // Rows 256..319 of B (32 KB on) into accumulator columns 256..319.
+            if constexpr (BN == 320)
+              umma_bf16(d_tmem + 256, da0 + off + 2 * k, db0 + off + ((256 * 128) >> 4) + 2 * k, idesc64,
+                        (kb | k) != 0);
+          }
           umma_commit(empty_bar(stage));
           ++fills;
           if (++stage == C::STAGES) {
@@ -402,8 +420,10 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
         }
         if (!ok) break;
         umma_commit(tfull_bar(acc));
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        if (++acc == kAccs) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
       }
       consumed_fills = fills;
       // All MMAs of this CTA complete before TMEM is released.
@@ -455,7 +475,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
 
 template <int BN, int EPI, int ASRC = kATma>
 int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmC,
-                  const GemmParams& p, cudaStream_t stream, const AGenParams* g = nullptr) {
+                  const GemmParams& p, cudaStream_t stream, const AGenParams* g = nullptr,
+                  const CUtensorMap* tmB64 = nullptr) {
   using C = GemmCfg<BN, ASRC>;
   if (allow_smem(reinterpret_cast<const void*>(gemm_kernel<BN, EPI, ASRC>), C::SMEM_BYTES) != cudaSuccess)
     return DS_VIT_ECUDA;
@@ -463,7 +484,7 @@ int launch_gemm_t(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensor
   const int grid = tiles < num_sms() ? tiles : num_sms();
   static const AGenParams none{};
   const cudaError_t e = launch_pdl(gemm_kernel<BN, EPI, ASRC>, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES,
-                                   stream, tmA, tmB, tmC, p, g ? *g : none);
+                                   stream, tmA, tmB, tmC, tmB64 ? *tmB64 : tmB, p, g ? *g : none);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
@@ -547,13 +568,30 @@ int gemm_bn(int M, int N) {
 }
 
 bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k) {
-  return make_tmap_bf16(&m->bn256, w, n, k, 256) && make_tmap_bf16(&m->bn128, w, n, k, 128);
+  return make_tmap_bf16(&m->bn256, w, n, k, 256) && make_tmap_bf16(&m->bn128, w, n, k, 128) &&
+         make_tmap_bf16(&m->bn64, w, n, k, 64);
+}
+
+// 320-wide tiles where they fit one round and the 256-wide choice needs two
+// or more (the merger linears at about a thousand tokens: 128 tiles against
+// 160 one-CTA or 80 paired 256-wide ones on 152 SMs).
+bool prefer_bn320(int M, int N) {
+  if (N % 320 != 0 || gemm_bn(M, N) != 256) return false;
+  const int sms = num_sms();
+  const int tiles320 = ((M + 127) / 128) * (N / 320);
+  const int tiles_pair = ((M + 255) / 256) * (N / 256);
+  return tiles320 <= sms && tiles_pair > sms / 2;
 }
 
 int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& tmC, int M, int N,
                 int K, const bf16* bias, bf16* out, int epi, const int* rowpos,
                 const float* rope_cs, int* status, cudaStream_t stream) {
   if (M <= 0 || K <= 0 || K % 64 != 0 || N % 128 != 0) return DS_VIT_EINVAL;
+  if ((epi == kEpiBias || epi == kEpiBiasGelu) && prefer_bn320(M, N)) {
+    const GemmParams p{M, N, K, out, bias, rowpos, rope_cs, status, tile_order(M, K)};
+    return epi == kEpiBias ? launch_gemm_t<320, kEpiBias>(tmA, B.bn256, tmC, p, stream, nullptr, &B.bn64)
+                           : launch_gemm_t<320, kEpiBiasGelu>(tmA, B.bn256, tmC, p, stream, nullptr, &B.bn64);
+  }
   // Where 256-wide tiles keep the SMs busy: 256 x 256 tiles on 2-CTA clusters
   // (a third less operand traffic per stage, six stages).
   if (N % 256 == 0 && gemm_bn(M, N) == 256) {
@@ -597,6 +635,8 @@ int launch_gemm_agen(int asrc, const AGenParams& g, const WeightMap& B, const CU
       !(asrc == kAMerge && K == 9216 && epi == kEpiBiasGelu))
     return DS_VIT_EINVAL;
   GemmParams p{M, N, K, out, bias, nullptr, nullptr, status, tile_order(M, K)};
+  if (asrc == kAMerge && prefer_bn320(M, N))
+    return launch_gemm_t<320, kEpiBiasGelu, kAMerge>(B.bn256, B.bn256, tmC, p, stream, &g, &B.bn64);
   const bool narrow = gemm_bn(M, N) == 128;
   const CUtensorMap& tmB = narrow ? B.bn128 : B.bn256;
   if (asrc == kAPixels)

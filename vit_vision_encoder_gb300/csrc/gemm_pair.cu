@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
   using C = PairCfg;
   constexpr int BN = 256;
+  constexpr uint32_t kAccs = 2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

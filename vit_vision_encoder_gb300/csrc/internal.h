@@ -70,6 +70,7 @@ cudaError_t allow_smem(const void* kernel, int bytes);
 struct WeightMap {
   CUtensorMap bn256;   // box 256 rows
   CUtensorMap bn128;   // box 128 rows
+  CUtensorMap bn64;    // box 64 rows (the last rows of a 320-row tile)
 };
 bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k);
 

@@ -59,6 +59,9 @@ GEMM_CASES = [
     # K = 4096; M = 4200, whose last tile's second 128-row half lies wholly past
     # M; the second merger linear's K = N = 5120.
     (3840, 4096, 1024, "resid"), (4200, 2048, 1024, "gelu"), (4200, 4096, 1024, "resid"),
+    # The out-projection shape with a ragged last tile: residual rows by TMA,
+    # 4 valid rows in the last tile's first half, none in its second.
+    (4100, 1024, 1024, "resid"), (9216, 1024, 1024, "resid"),
     # The merger linears' width at about a thousand rows: 320-wide tiles in one
     # round (two MMAs per K step, a 256-row and a 64-row B box); ragged M.
     (1024, 5120, 5120, "bias"), (1100, 2048, 5120, "gelu"), (1000, 1024, 5120, "bias"),

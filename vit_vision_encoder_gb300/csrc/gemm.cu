@@ -76,6 +76,7 @@ struct GemmCfg {
   // tiles (one row per thread) and 14-15 idle: 16 warps keep every SM
   // sub-partition within 4 x 32 x 128 registers.
   static constexpr int THREADS = (ASRC == kATma ? EPI_WARPS + 2 : 16) * 32;
+  static constexpr int BAR_RESID = 0;                          // the residual comes in registers here
 };
 static_assert(GemmCfg<256>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128>::SMEM_BYTES <= 232448, "shared memory");
@@ -280,6 +281,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
                 const GemmParams p, const __grid_constant__ AGenParams g) {
   using C = GemmCfg<BN, ASRC>;
   constexpr uint32_t kAccs = C::ACCS;
+  constexpr bool kResidTma = false;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));

@@ -33,33 +33,48 @@ namespace {
 
 #include "gemm_common.cuh"
 
-struct PairCfg {
+// RESID: the residual epilogue of a short-K GEMM (the out-projection, K =
+// 1024): its eight warps each load the tile's residual rows by TMA into four
+// staging chunks (32 rows x 32 columns, the store layout) and write the result
+// back in place; that buffer takes the room of one operand stage.  Per-thread
+// residual loads issued at a tile's start (4096 per SM) held up the TMA
+// producer for about 2 us per tile; with two tiles per pair that was a sixth
+// of the kernel.  Long-K GEMMs (FC2, K = 4096) keep six stages, which their
+// main loop needs more, and load the residual into registers.
+template <bool RESID>
+struct PairCfgT {
   static constexpr int BM = 128;                               // rows per CTA
   static constexpr int TILE_M = 256;                           // rows per tile
   static constexpr int BK = 64;
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = 128 * BK * 2;                 // this CTA's half of B
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = RESID ? 5 : 6;
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 32 * 2;
+  static constexpr int STG_PER_WARP = RESID ? 4 : 2;           // chunks of one tile / double buffer
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
-  static constexpr int OFF_BIAS = OFF_STG + EPI_WARPS * 2 * STG_BYTES;
+  static constexpr int OFF_BIAS = OFF_STG + EPI_WARPS * STG_PER_WARP * STG_BYTES;
   static constexpr int OFF_BAR = OFF_BIAS + 2 * 256 * 2;
   static constexpr int SMEM_BYTES = OFF_BAR + 256 + 1024;
   static constexpr int TMEM_COLS = 512;                        // two 256-column accumulators
   static constexpr int THREADS = (EPI_WARPS + 2) * 32;
+  static constexpr int BAR_RESID = 2 * STAGES + 5;             // one residual barrier per epilogue warp
 };
-static_assert(PairCfg::SMEM_BYTES <= 232448, "shared memory");
-static_assert(2 * PairCfg::STAGES + 5 <= 31, "barrier slots");
+using PairCfg = PairCfgT<false>;
+static_assert(PairCfgT<false>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(PairCfgT<true>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(PairCfgT<false>::BAR_RESID <= 31 && PairCfgT<true>::BAR_RESID + 8 <= 31, "barrier slots");
 
-template <int EPI>
+template <int EPI, bool RESID_TMA>
 __global__ void __launch_bounds__(PairCfg::THREADS, 1)
     gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                      const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
-  using C = PairCfg;
+  static_assert(!RESID_TMA || EPI == kEpiBiasResid, "TMA residual with the residual epilogue only");
+  using C = PairCfgT<RESID_TMA>;
   constexpr int BN = 256;
   constexpr uint32_t kAccs = 2;
+  constexpr bool kResidTma = RESID_TMA;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -92,6 +107,8 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
       mbar_init(tempty_bar(a), 2 * C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    if constexpr (kResidTma)
+      for (int w = 0; w < C::EPI_WARPS; ++w) mbar_init(bar0 + 8u * (C::BAR_RESID + w), 1);
     fence_barrier_init();
   }
   if (warp == 8 && lane == 0) {
@@ -230,7 +247,7 @@ __global__ void __launch_bounds__(PairCfg::THREADS, 1)
 
 // Clusters of two CTAs of `kernel` that fit on the device at once (0 if none
 // or the query fails); cached per kernel and device.
-int max_active_pairs(const void* kernel) {
+int max_active_pairs(const void* kernel, int smem_bytes) {
   static std::mutex mu;
   static std::map<std::pair<const void*, int>, int> cache;
   int dev = 0;
@@ -242,7 +259,7 @@ int max_active_pairs(const void* kernel) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * num_sms());
   cfg.blockDim = dim3(PairCfg::THREADS);
-  cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+  cfg.dynamicSmemBytes = smem_bytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -259,22 +276,23 @@ int max_active_pairs(const void* kernel) {
   return n;
 }
 
-template <int EPI>
+template <int EPI, bool RESID_TMA = false>
 int launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB128, const CUtensorMap& tmC, const GemmParams& p,
                   cudaStream_t stream) {
-  const void* kfn = reinterpret_cast<const void*>(gemm_pair_kernel<EPI>);
-  if (allow_smem(kfn, PairCfg::SMEM_BYTES) != cudaSuccess) return DS_VIT_ECUDA;
-  const int max_pairs = max_active_pairs(kfn);
+  using C = PairCfgT<RESID_TMA>;
+  const void* kfn = reinterpret_cast<const void*>(gemm_pair_kernel<EPI, RESID_TMA>);
+  if (allow_smem(kfn, C::SMEM_BYTES) != cudaSuccess) return DS_VIT_ECUDA;
+  const int max_pairs = max_active_pairs(kfn, C::SMEM_BYTES);
   if (max_pairs <= 0) return kGemmNoPair;
   // As few pairs as give the same number of rounds over the tiles: the same
   // time with less contention for L2 and power.
-  const int tiles = ((p.M + PairCfg::TILE_M - 1) / PairCfg::TILE_M) * (p.N / 256);
+  const int tiles = ((p.M + C::TILE_M - 1) / C::TILE_M) * (p.N / 256);
   const int rounds = (tiles + max_pairs - 1) / max_pairs;
   const int pairs = (tiles + rounds - 1) / rounds;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(PairCfg::THREADS);
-  cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+  cfg.blockDim = dim3(C::THREADS);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -285,7 +303,7 @@ int launch_pair_t(const CUtensorMap& tmA, const CUtensorMap& tmB128, const CUten
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI>, tmA, tmB128, tmC, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_pair_kernel<EPI, RESID_TMA>, tmA, tmB128, tmC, p);
   if (e != cudaSuccess) cudaGetLastError();
   return e == cudaSuccess ? DS_VIT_OK : DS_VIT_ECUDA;
 }
@@ -300,7 +318,9 @@ int launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB128, const CU
   switch (epi) {
     case kEpiBias: return launch_pair_t<kEpiBias>(tmA, tmB128, tmC, p, stream);
     case kEpiBiasGelu: return launch_pair_t<kEpiBiasGelu>(tmA, tmB128, tmC, p, stream);
-    case kEpiBiasResid: return launch_pair_t<kEpiBiasResid>(tmA, tmB128, tmC, p, stream);
+    case kEpiBiasResid:
+      return K <= 1024 ? launch_pair_t<kEpiBiasResid, true>(tmA, tmB128, tmC, p, stream)
+                       : launch_pair_t<kEpiBiasResid>(tmA, tmB128, tmC, p, stream);
     case kEpiQkvRope: return launch_pair_t<kEpiQkvRope>(tmA, tmB128, tmC, p, stream);
     case kEpiSwiglu: return launch_pair_t<kEpiSwiglu>(tmA, tmB128, tmC, p, stream);
     case kEpiQkvRope72: return launch_pair_t<kEpiQkvRope72>(tmA, tmB128, tmC, p, stream);

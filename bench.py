@@ -613,8 +613,31 @@ def main():
         dv.layout(GH, GW, cfg["image_token_id"], base)
         dv.overlay(hidden, [(base, GH, GW, 0)], out, sentinel)
 
+    # Throughput steps alternate between two streams, each with its own encoder
+    # workspace, output and prompt buffer, so one encode's sparse start and end
+    # (patch projection, merger, overlay) overlap the other's kernels, as a
+    # server would run consecutive requests.
+    enc_b = dv.Encoder(dw, cfg)
+    encs = (enc, enc_b)
+    outs = (out, torch.empty_like(out))
+    hiddens = (hidden, hidden.clone())
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+    def steps2(n):
+        cur = torch.cuda.current_stream()
+        for st in streams:
+            st.wait_stream(cur)
+        for i in range(n):
+            with torch.cuda.stream(streams[i % 2]):
+                encs[i % 2].encode([img], out=outs[i % 2])
+                dv.layout(GH, GW, cfg["image_token_id"], base)
+                dv.overlay(hiddens[i % 2], [(base, GH, GW, 0)], outs[i % 2], sentinel)
+        for st in streams:
+            cur.wait_stream(st)
+
     for _ in range(args.warmup):
         step()
+    steps2(2)
     torch.cuda.synchronize()
 
     # CUDA events around every kernel launch of every timed step.
@@ -636,8 +659,7 @@ def main():
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
-    for s in range(args.steps):
-        step()
+    steps2(args.steps)
     t1.record()
     torch.cuda.synchronize()
     if world > 1:
@@ -657,9 +679,9 @@ def main():
         step()
     torch.cuda.synchronize()
     enc.detach_timer()
-    status = enc.status()
-    if status != dv.OK:
-        raise RuntimeError(f"device status {status}")
+    for e in encs:
+        if e.status() != dv.OK:
+            raise RuntimeError(f"device status {e.status()}")
 
     per_kind = {}
     n_launch = 0
@@ -678,21 +700,37 @@ def main():
     tmax, value = aggregate(elapsed, N_TOK * args.steps, world)
 
     # End to end through the host-buffer entry point: pinned pixels in, pinned
-    # embeddings out, both copies inside the timed region.
-    hin = torch.from_numpy(img_np).pin_memory()
-    hout = torch.empty((N_TOK, 5120), dtype=torch.bfloat16).pin_memory()
-    for _ in range(args.warmup):
-        enc.encode_host([hin], hout)
+    # embeddings out, both copies inside the timed region.  Steps alternate
+    # between two streams, each with its own encoder workspace and host
+    # buffers, so one step's copies overlap the other's kernels (as a server
+    # would run consecutive requests).
+    hins = [torch.from_numpy(img_np).pin_memory() for _ in range(2)]
+    houts = [torch.empty((N_TOK, 5120), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+
+    def e2e_steps(n):
+        cur = torch.cuda.current_stream()
+        for st in streams:
+            st.wait_stream(cur)
+        for i in range(n):
+            with torch.cuda.stream(streams[i % 2]):
+                encs[i % 2].encode_host([hins[i % 2]], houts[i % 2])
+            dv.layout(GH, GW, cfg["image_token_id"], base)
+        for st in streams:
+            cur.wait_stream(st)
+
+    e2e_steps(max(args.warmup, 2))
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.steps):
-        enc.encode_host([hin], hout)
-        dv.layout(GH, GW, cfg["image_token_id"], base)
+    e2e_steps(args.steps)
     e1.record()
     torch.cuda.synchronize()
+    for e in encs:
+        if e.status() != dv.OK:
+            raise RuntimeError(f"device status {e.status()}")
+    enc_b.close()
     _, e2e_value = aggregate(e0.elapsed_time(e1) / 1e3, N_TOK * args.steps, world)
 
     pk = peaks()
@@ -715,6 +753,9 @@ def main():
                                "(hidden 1024, 16x64 heads, MLP 4096), 3x3 merge -> 1024 tokens x 5120, "
                                "layout (1058 rows) + overlay into a 4096x5120 prompt buffer",
                    "images_per_step": 1, "parallelism": f"replicas x{world}",
+                   "streams": "steps alternate between two streams (own workspace, output and prompt "
+                              "buffer each), so consecutive encodes overlap; per-kernel times and the "
+                              "roofline come from a single-stream pass",
                    "l2": "no flush: per-step working set above L2 (0.95 GB of weights streamed per "
                          "step, 189 MB of activations; L2 129 MB)",
                    "weights": "random N(0,0.02), seed 1000"},
@@ -730,7 +771,8 @@ def main():
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": IMG_H * IMG_W * 3,
                 "d2h_bytes_per_step": N_TOK * 5120 * 2,
-                "api": "ds_vit_encode_batch_host (pinned pixels in, pinned embeddings out) + ds_vit_layout"},
+                "api": "ds_vit_encode_batch_host (pinned pixels in, pinned embeddings out) + ds_vit_layout; "
+                       "steps alternate between two streams, each with its own workspace"},
         "clocks": clk,
     }
     if not args.skip_workloads:

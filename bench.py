@@ -365,7 +365,9 @@ def official_workload(pk, reps: int = 5):
 
 def other_workloads(dw, cfg, pk, reps: int = 5):
     """images/s, merged tokens/s and the fraction of the bf16 peak on the other
-    synthetic workloads (CUDA events around the encode only)."""
+    synthetic workloads (CUDA events around the encode only): one stream, and
+    (except the aspect-ratio workload, whose protocol is one stream) two
+    encodes in flight on two streams."""
     import torch
 
     import workloads as WL
@@ -396,6 +398,38 @@ def other_workloads(dw, cfg, pk, reps: int = 5):
                      "ms_per_encode": round(sec * 1e3, 4), "images_per_s": round(len(imgs) / sec, 2),
                      "tokens_per_s": round(T / sec, 1), "tflops": round(fl / sec / 1e12, 1),
                      "frac_of_peak": round(fl / sec / 1e12 / pk["tc"], 3)}
+        if name != "aspect":
+            # The same encodes alternating between two streams (own workspace
+            # and output each), as the headline step runs; the aspect-ratio
+            # workload's protocol is one stream.
+            enc_b = dv.Encoder(dw, cfg, n_layers=wl["n_layers"])
+            encs, outs = (enc, enc_b), (out, torch.empty_like(out))
+            streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+
+            def two(n):
+                cur = torch.cuda.current_stream()
+                for st in streams:
+                    st.wait_stream(cur)
+                for i in range(n):
+                    with torch.cuda.stream(streams[i % 2]):
+                        encs[i % 2].encode(imgs, out=outs[i % 2])
+                for st in streams:
+                    cur.wait_stream(st)
+
+            two(2)
+            torch.cuda.synchronize()
+            n2 = 2 * runs
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            two(n2)
+            e1.record()
+            torch.cuda.synchronize()
+            sec2 = e0.elapsed_time(e1) / 1e3 / n2
+            res[name]["two_streams"] = {"ms_per_encode": round(sec2 * 1e3, 4), "tokens_per_s": round(T / sec2, 1),
+                                        "frac_of_peak": round(fl / sec2 / 1e12 / pk["tc"], 3)}
+            if enc_b.status() != dv.OK:
+                raise RuntimeError(f"device status after {name} (second stream)")
+            enc_b.close()
         if enc.status() != dv.OK:
             raise RuntimeError(f"device status after {name}")
         enc.close()

@@ -90,6 +90,35 @@ def test_repeat_is_deterministic(dv, enc2):
     assert torch.equal(a, b)
 
 
+def test_two_streams_match_one(dv, enc2, w2):
+    """Two prepared handles encoding concurrently on two streams (each with
+    its own workspace and output, as the throughput measurement runs) give
+    the one-stream embeddings bit for bit: nothing is shared between handles."""
+    imgs = [WL.uniform_image(h, w, seed=400 + i) for i, (h, w) in enumerate([(350, 294), (210, 1008)])]
+    d = [torch.from_numpy(im).cuda() for im in imgs]
+    ref, offs = _run(dv, enc2, imgs)
+    ref = ref.clone()
+    enc_b = dv.Encoder(dv.weights_to_device(w2), WL.MODEL)
+    try:
+        encs = (enc2, enc_b)
+        outs = [torch.zeros_like(ref) for _ in range(4)]
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        cur = torch.cuda.current_stream()
+        for st in streams:
+            st.wait_stream(cur)
+        for i in range(4):
+            with torch.cuda.stream(streams[i % 2]):
+                encs[i % 2].encode(d, out=outs[i])
+        for st in streams:
+            cur.wait_stream(st)
+        torch.cuda.synchronize()
+        assert enc2.status() == dv.OK and enc_b.status() == dv.OK
+        for o in outs:
+            assert torch.equal(o, ref)
+    finally:
+        enc_b.close()
+
+
 def test_host_buffers_match_device(dv, enc2):
     imgs = [WL.uniform_image(h, w, seed=300 + i) for i, (h, w) in enumerate([(84, 84), (168, 98)])]
     dev_out, offs = _run(dv, enc2, imgs)

@@ -34,6 +34,10 @@ CASES = [
     ((3, 700), "uniform", 9),        # one axis far below the other
     ((1344, 1000), "gradient", 10),  # height kept (1344 = 32 units), width resized
     ((20000, 100), "gradient", 11),  # 200:1, no aspect clamp
+    ((4500, 6000), "uniform", 12),   # downscale by 4: 17-tap filters (generic horizontal pass)
+    ((2640, 112), "gradient", 13),   # width kept, height resized from the input's 336-byte rows
+    ((2136, 140), "uniform", 14),    # width kept, 420-byte rows (not 16-byte multiples)
+    ((1200, 5000), "gradient", 15),  # wide downscale: 21 column blocks with a ragged last one
 ]
 
 
@@ -46,6 +50,19 @@ def test_preprocess_matches_oracle_bytes(dv, hw, kind, seed):
     assert plan["Hc"] == ref.shape[0] and plan["Wc"] == ref.shape[1]
     got = canvas.cpu().numpy()
     assert np.array_equal(got, ref), f"{int((got != ref).sum())} bytes differ"
+
+
+@pytest.mark.parametrize("hw", [(2640, 112), (1000, 333)])
+def test_preprocess_unaligned_source(dv, hw):
+    """An image that starts one byte into its allocation (a view): the passes
+    that read 16-byte words of the source must not be taken."""
+    img = WL.make_image(hw[0], hw[1], "uniform", 16)
+    flat = torch.empty(img.size + 1, dtype=torch.uint8, device="cuda")
+    view = flat[1:].view(hw[0], hw[1], 3)
+    view.copy_(torch.from_numpy(img).cuda())
+    canvas, _ = dv.preprocess(view)
+    torch.cuda.synchronize()
+    assert np.array_equal(canvas.cpu().numpy(), PP.preprocess(img))
 
 
 def test_preprocess_photo_full_size(dv):

@@ -9,10 +9,11 @@
 //
 // One CTA = one (image, 256 query rows, head), as two 128-row query tiles A
 // and B that share every K/V tile.  Warps 0-7 run the softmax of tile A and
-// warps 8-15 that of tile B: two threads per query row (TMEM lane = row), one
-// per 64-key half of the score tile (read with one tcgen05.ld.red that also
-// returns the half-row maximum), which exchange their half-row maxima
-// through shared memory (an mbarrier per lane quadrant), so every SM
+// warps 8-15 that of tile B: a warp takes 16 query rows (TMEM lanes) with two
+// threads per row, one per 64-key half of the score tile, read with one
+// tcgen05.ld.red of the 16x32bx2 shape (threads t and t + 16 on the same
+// lane, 64 columns apart) that also returns the half-row maximum; the two
+// halves exchange their maxima and sums by warp shuffle.  Every SM
 // sub-partition runs four softmax warps.  Warp 16 loads Q once and streams K/V
 // tiles of 128 rows through a 4-stage TMA ring; warp 17 issues the MMAs of
 // tile A and warp 18 those of tile B, so the two tiles proceed independently
@@ -67,8 +68,7 @@ enum : int {
   kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
   kBarDrain = kBarPvDone + 2,          // [2]
-  kBarXch = kBarDrain + 2,             // [2 tiles][4 quadrants]: half-row exchange
-  kBarTurn = kBarXch + 8,              // [2]: tile X finished the math of a step
+  kBarTurn = kBarDrain + 2,            // [2]: tile X finished the math of a step
   kBarCount = kBarTurn + 2
 };
 static_assert(kBarCount <= 30, "barrier area");
@@ -143,7 +143,6 @@ __global__ void __maxnreg__(96)
       mbar_init(bar(kBarPFull + x), 256);
       mbar_init(bar(kBarPvDone + x), 1);
       mbar_init(bar(kBarDrain + x), 1);
-      for (int q = 0; q < 4; ++q) mbar_init(bar(kBarXch + 4 * x + q), 64);
       mbar_init(bar(kBarTurn + x), 256);
     }
     fence_barrier_init();
@@ -161,9 +160,6 @@ __global__ void __maxnreg__(96)
   grid_dep_wait();
 
   __shared__ int kv_consumed[2];
-  // Half-row values exchanged between the two threads of a row:
-  // [exchange parity][tile][half][row].
-  __shared__ float xch[2][2][2][kTile];
   int kv_issued = 0;
   bool q_issued = false;
 
@@ -235,23 +231,15 @@ __global__ void __maxnreg__(96)
     // ------------------------------------------------------------ softmax (warps 0-15)
     const int x = warp >> 3;                 // query tile A (0) or B (1)
     const int qd = warp & 3;                 // TMEM lane quadrant
-    const int h = (warp >> 2) & 1;           // 64-key half of the score tile
-    const int r = qd * 32 + lane;            // row inside the tile == TMEM lane
-    const uint32_t lane_sel = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;
-    const uint32_t tO = tmem + kTmemO + x * 64 + h * 32 + lane_sel;
-    const uint32_t tP = tmem + kTmemP + x * 64 + h * 32 + lane_sel;
-    const uint32_t xbar = bar(kBarXch + 4 * x + qd);
-    // Both threads of a row write their half's value, arrive, wait for the
-    // phase and read the other's; slot parity e alternates, so a slot is
-    // rewritten only after its reader has arrived at the next exchange.
-    auto exchange = [&](float v, int e, float* other) {
-      xch[e & 1][x][h][r] = v;
-      mbar_arrive(xbar);
-      if (!mbar_wait(xbar, e & 1, p.status)) return false;
-      *other = xch[e & 1][x][h ^ 1][r];
-      return true;
-    };
+    const int base = qd * 32 + ((warp >> 2) & 1) * 16;   // the warp's first row
+    const int h = lane >> 4;                 // 64-key half of the score tile
+    const int r = base + (lane & 15);        // row inside the tile == TMEM lane
+    // Addresses of the first half; the 16x32bx2 accesses put threads 16-31
+    // on the second (64 score columns, 32 O and P columns further on).
+    const uint32_t lane_sel = static_cast<uint32_t>(base) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_sel;
+    const uint32_t tO = tmem + kTmemO + x * 64 + lane_sel;
+    const uint32_t tP = tmem + kTmemP + x * 64 + lane_sel;
     const float c = p.scale_log2;
     const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
@@ -265,7 +253,7 @@ __global__ void __maxnreg__(96)
       tc_fence_after();
       uint32_t sr[64];
       // One load of the 64 scores that also reduces them to their maximum.
-      float m_half = tmem_ld64_max(tS, sr);
+      float m_half = tmem_ld64_max_x2<64>(tS, sr);
       tmem_wait_ld();
       m_half = tmem_after_wait(m_half);
       tc_fence_before();
@@ -289,11 +277,7 @@ __global__ void __maxnreg__(96)
         }
         m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      float m_other;
-      if (!exchange(m_half, j, &m_other)) {
-        ok = false;
-        break;
-      }
+      const float m_other = __shfl_xor_sync(0xFFFFFFFFu, m_half, 16);
       // Both threads of the row derive the same m_new and alpha.
       const float m_tile = fmaxf(m_half, m_other) * c;
       float m_new = m, alpha = 1.f;
@@ -326,26 +310,26 @@ __global__ void __maxnreg__(96)
         }
         tc_fence_after();
       }
-      tmem_st32(tP, pk);
+      tmem_st32_x2<32>(tP, pk);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
         uint32_t o[32];
-        tmem_ld32(tO, o);
+        tmem_ld32_x2<32>(tO, o);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO, o);
+        tmem_st32_x2<32>(tO, o);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + x));
       m = m_new;
     }
-    float l_other = 0.f;
-    if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
+    const float l_other = __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+    if (ok && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
       const float inv_l = 1.f / (l + l_other);
       uint32_t o[32];
-      tmem_ld32(tO, o);
+      tmem_ld32_x2<32>(tO, o);
       tmem_wait_ld();
       const int qrow = q0 + x * kTile + r;
       if (qrow < row0 + len) {

@@ -367,7 +367,8 @@ def other_workloads(dw, cfg, pk, reps: int = 5):
     """images/s, merged tokens/s and the fraction of the bf16 peak on the other
     synthetic workloads (CUDA events around the encode only): one stream, and
     (except the aspect-ratio workload, whose protocol is one stream) two
-    encodes in flight on two streams."""
+    encodes in flight on two streams, issued eagerly and replayed from CUDA
+    graphs recorded once per stream."""
     import torch
 
     import workloads as WL
@@ -427,6 +428,32 @@ def other_workloads(dw, cfg, pk, reps: int = 5):
             sec2 = e0.elapsed_time(e1) / 1e3 / n2
             res[name]["two_streams"] = {"ms_per_encode": round(sec2 * 1e3, 4), "tokens_per_s": round(T / sec2, 1),
                                         "frac_of_peak": round(fl / sec2 / 1e12 / pk["tc"], 3)}
+            # The same, each stream's encode recorded once as a CUDA graph and
+            # replayed (its own input copy, workspace and output).
+            imgs_b = [im.clone() for im in imgs]
+            graphs = [encs[0].graph(imgs, out=outs[0])[0], encs[1].graph(imgs_b, out=outs[1])[0]]
+
+            def two_graph(n):
+                cur = torch.cuda.current_stream()
+                for st in streams:
+                    st.wait_stream(cur)
+                for i in range(n):
+                    graphs[i % 2].launch(streams[i % 2])
+                for st in streams:
+                    cur.wait_stream(st)
+
+            two_graph(2)
+            torch.cuda.synchronize()
+            e0.record()
+            two_graph(n2)
+            e1.record()
+            torch.cuda.synchronize()
+            sec3 = e0.elapsed_time(e1) / 1e3 / n2
+            res[name]["two_streams_graph"] = {"ms_per_encode": round(sec3 * 1e3, 4),
+                                              "tokens_per_s": round(T / sec3, 1),
+                                              "frac_of_peak": round(fl / sec3 / 1e12 / pk["tc"], 3)}
+            for g in graphs:
+                g.close()
             if enc_b.status() != dv.OK:
                 raise RuntimeError(f"device status after {name} (second stream)")
             enc_b.close()
@@ -692,9 +719,29 @@ def main():
         for st in streams:
             cur.wait_stream(st)
 
+    # The same steps with each stream's encode recorded once as a CUDA graph
+    # (ds_vit_graph_create) on its own input, workspace and output, and
+    # replayed: every replay runs every kernel of the encode; only the host's
+    # launch calls are saved.  The overlay is launched directly each step.
+    imgs_g = (img, img.clone())
+    graphs = [encs[i].graph([imgs_g[i]], out=outs[i])[0] for i in range(2)]
+
+    def steps2_graph(n):
+        cur = torch.cuda.current_stream()
+        for st in streams:
+            st.wait_stream(cur)
+        for i in range(n):
+            with torch.cuda.stream(streams[i % 2]):
+                graphs[i % 2].launch(streams[i % 2])
+                dv.layout(GH, GW, cfg["image_token_id"], base)
+                dv.overlay(hiddens[i % 2], [(base, GH, GW, 0)], outs[i % 2], sentinel)
+        for st in streams:
+            cur.wait_stream(st)
+
     for _ in range(args.warmup):
         step()
     steps2(2)
+    steps2_graph(max(args.warmup, 2))
     torch.cuda.synchronize()
 
     # CUDA events around every kernel launch of every timed step.
@@ -716,13 +763,21 @@ def main():
     torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t0.record()
-    steps2(args.steps)
+    steps2_graph(args.steps)
     t1.record()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     elapsed = t0.elapsed_time(t1) / 1e3
     clk = clocks.stop()
+
+    # The same K steps issued eagerly (every kernel launched from the host).
+    torch.cuda.synchronize()
+    t0.record()
+    steps2(args.steps)
+    t1.record()
+    torch.cuda.synchronize()
+    eager_elapsed = t0.elapsed_time(t1) / 1e3
 
     # Timed region 2 (per-kernel times, the roofline): the same K steps with CUDA
     # events recorded around every kernel launch on the encode's stream.
@@ -755,6 +810,7 @@ def main():
     gpu_launches = n_launch * args.steps
 
     tmax, value = aggregate(elapsed, N_TOK * args.steps, world)
+    eager_tmax, eager_value = aggregate(eager_elapsed, N_TOK * args.steps, world)
 
     # End to end through the host-buffer entry point: pinned pixels in, pinned
     # embeddings out, both copies inside the timed region.  Steps alternate
@@ -764,13 +820,18 @@ def main():
     hins = [torch.from_numpy(img_np).pin_memory() for _ in range(2)]
     houts = [torch.empty((N_TOK, 5120), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
 
+    # Each stream's host-buffer encode recorded once as a CUDA graph
+    # (ds_vit_graph_create with host = 1): every replay copies the pixels in,
+    # encodes and copies the embeddings out.
+    hgraphs = [encs[i].graph_host([hins[i]], houts[i])[0] for i in range(2)]
+
     def e2e_steps(n):
         cur = torch.cuda.current_stream()
         for st in streams:
             st.wait_stream(cur)
         for i in range(n):
             with torch.cuda.stream(streams[i % 2]):
-                encs[i % 2].encode_host([hins[i % 2]], houts[i % 2])
+                hgraphs[i % 2].launch(streams[i % 2])
             dv.layout(GH, GW, cfg["image_token_id"], base)
         for st in streams:
             cur.wait_stream(st)
@@ -787,6 +848,8 @@ def main():
     for e in encs:
         if e.status() != dv.OK:
             raise RuntimeError(f"device status {e.status()}")
+    for g in graphs + hgraphs:
+        g.close()
     enc_b.close()
     _, e2e_value = aggregate(e0.elapsed_time(e1) / 1e3, N_TOK * args.steps, world)
 
@@ -813,6 +876,9 @@ def main():
                    "streams": "steps alternate between two streams (own workspace, output and prompt "
                               "buffer each), so consecutive encodes overlap; per-kernel times and the "
                               "roofline come from a single-stream pass",
+                   "launch": "each stream's encode recorded once as a CUDA graph (ds_vit_graph_create) "
+                             "and replayed every step (all kernels run each replay); the overlay is "
+                             "launched directly; the same steps issued eagerly are under 'eager'",
                    "l2": "no flush: per-step working set above L2 (0.95 GB of weights streamed per "
                          "step, 189 MB of activations; L2 129 MB)",
                    "weights": "random N(0,0.02), seed 1000"},
@@ -825,11 +891,15 @@ def main():
                      "frac_of_burst": attn_tflops / pk["bf16"], "frac_of_sustained": attn_tflops / pk["bf16_sus"],
                      "flop_per_launch": KIND_FLOP["attention"], "traffic": measured_traffic()},
         "kernels": kernels,
+        "eager": {"value": eager_value, "ms_per_step": eager_tmax / args.steps * 1e3,
+                  "launch": "every kernel launched from the host (ds_vit_encode_batch per step)"},
         "gpu_launches": gpu_launches,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": IMG_H * IMG_W * 3,
                 "d2h_bytes_per_step": N_TOK * 5120 * 2,
-                "api": "ds_vit_encode_batch_host (pinned pixels in, pinned embeddings out) + ds_vit_layout; "
-                       "steps alternate between two streams, each with its own workspace"},
+                "api": "ds_vit_encode_batch_host (pinned pixels in, pinned embeddings out) recorded once per "
+                       "stream as a CUDA graph (ds_vit_graph_create, host = 1; both copies and the encode in "
+                       "every replay) + ds_vit_layout; steps alternate between two streams, each with its "
+                       "own workspace"},
         "clocks": clk,
     }
     if not args.skip_workloads:

@@ -245,6 +245,36 @@ int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* con
                              int64_t* tok_offsets, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * ds_vit_graph_create / ds_vit_graph_launch / ds_vit_graph_destroy: one encode
+ * recorded once as a CUDA graph and replayed.  The pages have no counterpart:
+ * an encode is a few hundred kernel launches (seven per block), and on small
+ * images the host's launch calls take about as long as the device work, so a
+ * serving loop that encodes the same image sizes again records the encode
+ * once and replays it.
+ *   ds_vit_graph_create records ds_vit_encode_batch (host == 0) or
+ *   ds_vit_encode_batch_host (host != 0; pixels and out then in page-locked
+ *   host memory) with exactly these arguments on an internal stream, runs
+ *   nothing, and stores an opaque executable-graph handle in *graph;
+ *   tok_offsets is filled as by the recorded call.  Every replay repeats the
+ *   whole encode (all its kernels and, for host == 1, both copies) on the same
+ *   buffers: their contents may change between replays, their addresses and
+ *   the image sizes may not, and the buffers must outlive the handle.
+ *   Replays on different streams need different workspaces and outputs.  The
+ *   kernel timer (ds_vit_set_kernel_timer) must be detached while recording.
+ *   Errors: DS_VIT_EINVAL for a null p or graph (nothing else is touched),
+ *   the recorded call's own error code (nothing is kept), DS_VIT_ECUDA when
+ *   the stream, the recording or the instantiation fails.
+ *   ds_vit_graph_launch queues one replay on `stream` (DS_VIT_EINVAL for a null
+ *   handle, DS_VIT_ECUDA when the launch fails); ds_vit_graph_destroy frees the
+ *   handle (the caller ensures no replay is still running on the device).
+ */
+int ds_vit_graph_create(const ds_vit_prepared* p, int host, int n, const uint8_t* const* pixels,
+                        const int32_t* H, const int32_t* W, void* out, int64_t* tok_offsets, void* ws,
+                        size_t ws_bytes, void** graph);
+int ds_vit_graph_launch(void* graph, void* stream);
+int ds_vit_graph_destroy(void* graph);
+
+/*
  * ds_vit_encode_noalloc: ds_vit_encode for callers that cannot allocate device
  * memory when they encode (an application that owns the whole device budget
  * through its own pool, a latency-critical loop that must not pay cudaMalloc's

@@ -37,6 +37,16 @@ def test_exports_every_declared_symbol(dv):
     assert set(names) == set(dv.SIGNATURES)
 
 
+def test_graph_calls_reject_null_handles(dv):
+    """The graph entry points check their handles before any CUDA call."""
+    g = C.c_void_p(123)
+    assert dv.lib.ds_vit_graph_create(None, 0, 0, None, None, None, None, None, None, 0, C.byref(g)) == dv.EINVAL
+    assert g.value == 123                     # untouched: rejected before anything is written
+    assert dv.lib.ds_vit_graph_create(C.c_void_p(1), 0, 0, None, None, None, None, None, None, 0, None) == dv.EINVAL
+    assert dv.lib.ds_vit_graph_launch(None, None) == dv.EINVAL
+    assert dv.lib.ds_vit_graph_destroy(None) == dv.EINVAL
+
+
 def test_strerror(dv):
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert dv.lib.ds_vit_strerror(code)

@@ -129,6 +129,74 @@ def test_host_buffers_match_device(dv, enc2):
     assert np.array_equal(offs, offs2) and torch.equal(hout, dev_out.cpu())
 
 
+def test_graph_replays_the_encode(dv, enc2):
+    """An encode recorded as a graph (ds_vit_graph_create) and replayed gives
+    the direct encode's embeddings bit for bit, and recomputes them: after new
+    pixels are written into the same buffers, a replay matches a direct encode
+    of the new images.  Replays alternate between two graphs on two streams."""
+    sizes = [(350, 294), (84, 84)]
+    first = [torch.from_numpy(WL.uniform_image(h, w, seed=500 + i)).cuda() for i, (h, w) in enumerate(sizes)]
+    second = [torch.from_numpy(WL.uniform_image(h, w, seed=600 + i)).cuda() for i, (h, w) in enumerate(sizes)]
+    ref1, offs = enc2.encode(first)
+    ref1 = ref1.clone()
+    ref2, _ = enc2.encode(second)
+    ref2 = ref2.clone()
+    torch.cuda.synchronize()
+    bufs = [[im.clone() for im in first] for _ in range(2)]
+    graphs = []
+    try:
+        for b in bufs:
+            g, out, goffs = enc2.graph(b)
+            assert np.array_equal(goffs, offs)
+            graphs.append((g, out))
+        streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+        cur = torch.cuda.current_stream()
+        for st in streams:
+            st.wait_stream(cur)
+        for i in range(4):
+            graphs[i % 2][0].launch(streams[i % 2])
+        for st in streams:
+            cur.wait_stream(st)
+        torch.cuda.synchronize()
+        for _, out in graphs:
+            assert torch.equal(out, ref1)
+        for b in bufs:                       # same buffers, new contents
+            for dst, src in zip(b, second):
+                dst.copy_(src)
+        for g, _ in graphs:
+            g.launch()
+        torch.cuda.synchronize()
+        assert enc2.status() == dv.OK
+        for _, out in graphs:
+            assert torch.equal(out, ref2)
+    finally:
+        for g, _ in graphs:
+            g.close()
+
+
+def test_graph_host_buffers(dv, enc2):
+    """The host-buffer encode recorded as a graph: both copies and the encode
+    in every replay, page-locked buffers."""
+    imgs = [WL.uniform_image(h, w, seed=700 + i) for i, (h, w) in enumerate([(168, 98), (84, 84)])]
+    dev_out, offs = _run(dv, enc2, imgs)
+    hin = [torch.from_numpy(im).pin_memory() for im in imgs]
+    hout = torch.zeros((int(offs[-1]), 5120), dtype=torch.bfloat16).pin_memory()
+    g, goffs = enc2.graph_host(hin, hout)
+    try:
+        g.launch()
+        torch.cuda.synchronize()
+        assert np.array_equal(goffs, offs) and torch.equal(hout, dev_out.cpu())
+        new = [WL.uniform_image(h, w, seed=800 + i) for i, (h, w) in enumerate([(168, 98), (84, 84)])]
+        new_out, _ = _run(dv, enc2, new)
+        for dst, src in zip(hin, new):
+            dst.copy_(torch.from_numpy(src))
+        g.launch()
+        torch.cuda.synchronize()
+        assert torch.equal(hout, new_out.cpu())
+    finally:
+        g.close()
+
+
 def test_errors_write_nothing(dv, enc2):
     import ctypes as C
     img = torch.from_numpy(WL.uniform_image(84, 84, seed=5)).cuda()

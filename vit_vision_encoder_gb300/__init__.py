@@ -92,6 +92,10 @@ SIGNATURES = {
                                            _P_I64, _VP, _SZ, _VP]),
     "ds_vit_encode_debug": (C.c_int, [_VP, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,
                                       _VP, _SZ, _VP, _VP, _VP]),
+    "ds_vit_graph_create": (C.c_int, [_VP, C.c_int, C.c_int, C.POINTER(_VP), _P_I32, _P_I32, _VP, _P_I64,
+                                      _VP, _SZ, C.POINTER(_VP)]),
+    "ds_vit_graph_launch": (C.c_int, [_VP, _VP]),
+    "ds_vit_graph_destroy": (C.c_int, [_VP]),
     "ds_vit_overlay": (C.c_int, [_VP, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP, _VP]),
     "ds_vit_overlay_rows": (C.c_int, [_VP, _I64, _I32, _VP, _VP, _VP, _I64, _VP, _I64, _VP, _VP, _VP]),
     "ds_vit_overlay_chunk": (C.c_int, [_VP, _I64, _I64, _I32, C.POINTER(Span), C.c_int, _VP, _I64, _VP,
@@ -292,6 +296,37 @@ class Encoder:
               "ds_vit_encode_batch_host")
         return np.array(offs[:], dtype=np.int64)
 
+    def graph(self, images, out=None):
+        """Record one encode of `images` (uint8 CUDA tensors) into `out` as a
+        CUDA graph (ds_vit_graph_create); returns (EncodeGraph, out,
+        tok_offsets).  Each launch() repeats the whole encode on these
+        buffers, whose contents may change between launches."""
+        torch = _torch()
+        sizes = [(int(im.shape[0]), int(im.shape[1])) for im in images]
+        if out is None:
+            out = torch.empty((self.tokens(sizes), 5120), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(self.workspace_bytes(sizes), 16), dtype=torch.uint8, device="cuda")
+        return self._record(0, images, sizes, out, ws), out, self._last_offsets
+
+    def graph_host(self, images_host, out_host):
+        """As graph(), recording ds_vit_encode_batch_host: page-locked CPU
+        images in, page-locked CPU output out, both copies in every launch."""
+        torch = _torch()
+        sizes = [(int(im.shape[0]), int(im.shape[1])) for im in images_host]
+        ws = torch.empty(max(self.workspace_bytes(sizes, host=True), 16), dtype=torch.uint8, device="cuda")
+        return self._record(1, images_host, sizes, out_host, ws), self._last_offsets
+
+    def _record(self, host, images, sizes, out, ws):
+        n = len(sizes)
+        H, W = _i32([s[0] for s in sizes]), _i32([s[1] for s in sizes])
+        px = (C.c_void_p * n)(*[im.data_ptr() for im in images])
+        offs = (C.c_int64 * (n + 1))()
+        h = C.c_void_p()
+        check(lib.ds_vit_graph_create(self.handle, host, n, px, H, W, _ptr(out), offs, _ptr(ws), ws.numel(),
+                                      C.byref(h)), "ds_vit_graph_create")
+        self._last_offsets = np.array(offs[:], dtype=np.int64)
+        return EncodeGraph(h, (images, out, ws, self))
+
     def attach_timer(self, n_slots: int = 512):
         """Bracket every kernel of later encode calls with CUDA events; returns
         a callable giving [(kind, ms), ...] for the latest call (after a sync)."""
@@ -318,6 +353,29 @@ class Encoder:
 
     def status(self) -> int:
         return lib.ds_vit_device_status(self.handle, _stream())
+
+
+class EncodeGraph:
+    """An executable graph of one recorded encode; holds its buffers."""
+
+    def __init__(self, handle, keep):
+        self.handle, self._keep = handle, keep
+
+    def launch(self, stream=None):
+        torch = _torch()
+        st = C.c_void_p((stream or torch.cuda.current_stream()).cuda_stream)
+        check(lib.ds_vit_graph_launch(self.handle, st), "ds_vit_graph_launch")
+
+    def close(self):
+        if self.handle:
+            lib.ds_vit_graph_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class QwenEncoder:

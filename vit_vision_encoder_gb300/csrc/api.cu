@@ -510,6 +510,51 @@ int ds_vit_encode_batch_host(const ds_vit_prepared* p, int n, const uint8_t* con
   return DS_VIT_OK;
 }
 
+int ds_vit_graph_create(const ds_vit_prepared* p, int host, int n, const uint8_t* const* pixels,
+                        const int32_t* H, const int32_t* W, void* out, int64_t* tok_offsets, void* ws,
+                        size_t ws_bytes, void** graph) {
+  if (!p || !graph) return DS_VIT_EINVAL;
+  *graph = nullptr;
+  cudaStream_t st = nullptr;
+  DSV_CUDA(cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking));
+  if (cudaStreamBeginCapture(st, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    cudaStreamDestroy(st);
+    return DS_VIT_ECUDA;
+  }
+  const int rc = host ? ds_vit_encode_batch_host(p, n, pixels, H, W, out, tok_offsets, ws, ws_bytes, st)
+                      : encode_common(p, n, pixels, H, W, out, tok_offsets, ws, ws_bytes, nullptr, nullptr, st);
+  cudaGraph_t g = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(st, &g);
+  cudaStreamDestroy(st);
+  if (rc != DS_VIT_OK || ec != cudaSuccess || g == nullptr) {
+    if (g != nullptr) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return rc != DS_VIT_OK ? rc : DS_VIT_ECUDA;
+  }
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, g, 0);
+  cudaGraphDestroy(g);
+  if (ei != cudaSuccess) {
+    cudaGetLastError();
+    return DS_VIT_ECUDA;
+  }
+  *graph = exec;
+  return DS_VIT_OK;
+}
+
+int ds_vit_graph_launch(void* graph, void* stream) {
+  if (!graph) return DS_VIT_EINVAL;
+  DSV_CUDA(cudaGraphLaunch(static_cast<cudaGraphExec_t>(graph), static_cast<cudaStream_t>(stream)));
+  return DS_VIT_OK;
+}
+
+int ds_vit_graph_destroy(void* graph) {
+  if (!graph) return DS_VIT_EINVAL;
+  DSV_CUDA(cudaGraphExecDestroy(static_cast<cudaGraphExec_t>(graph)));
+  return DS_VIT_OK;
+}
+
 int ds_vit_overlay(void* hidden, int64_t n_hidden, int32_t width, const ds_vit_span* spans,
                    int n_spans, const void* embeds, int64_t n_embeds, const void* sentinel,
                    void* stream) {

@@ -52,9 +52,13 @@ GEMM_CASES = [
     (1, 64, 256, "bias"), (77, 640, 1024, "bias"), (300, 1024, 1024, "bias"),
     (1000, 1024, 4096, "gelu"), (513, 4096, 1024, "resid"), (169, 9216, 5120, "gelu"),
     (2000, 1024, 1024, "resid"),
-    # N % 256 == 128 with many rows (N = 1152 is the Qwen-style tower's hidden
-    # width; 128-wide tiles, ragged M in the second case).
-    (4096, 1152, 1152, "resid"), (3000, 1152, 1152, "bias"), (2500, 640, 1408, "gelu"),
+    # N = 1152 (the Qwen-style tower's hidden width, a multiple of 288 but not
+    # of 256): 288-wide tiles where they fit one round (two MMAs per K step, a
+    # 256-row and a 32-row B box; odd chunk count in the epilogue), ragged M in
+    # the second case, the tower's FC2 shape (K = 4608); 128-wide tiles where
+    # they do not (5000 rows: 160 tiles of 288) and for other widths.
+    (4096, 1152, 1152, "resid"), (3000, 1152, 1152, "bias"), (1700, 1152, 1152, "gelu"),
+    (4096, 4608, 1152, "resid"), (5000, 1152, 1152, "resid"), (2500, 640, 1408, "gelu"),
     # K >= 2048 with enough 256 x 256 tiles: the 2-CTA-cluster kernel.  FC2-like
     # K = 4096; M = 4200, whose last tile's second 128-row half lies wholly past
     # M; the second merger linear's K = N = 5120.

@@ -27,9 +27,10 @@
 // each 32x32 output chunk goes through a 64-byte-swizzled shared staging tile
 // (two per warp) and leaves by TMA store, which also clips rows past M.
 // 320-wide tiles (the merger linears, N = 5120, at sizes where 256-wide tiles
-// need a second, almost empty round) issue two MMAs per K step (N = 256 and
-// N = 64 into adjacent TMEM columns), load B as a 256-row and a 64-row box,
-// and keep one accumulator (320 of the 512 columns).
+// need a second, almost empty round) and 288-wide tiles (widths of 1152, which
+// otherwise take 128-wide tiles) issue two MMAs per K step (N = 256 and
+// N = 64 or 32 into adjacent TMEM columns), load B as a 256-row and a 64- or
+// 32-row box, and keep one accumulator (320 or 288 of the 512 columns).
 // Where 256-wide tiles are chosen and A comes by TMA, the 2-CTA-cluster
 // kernel runs instead (gemm_pair.cu, 256 x 256 tiles, same epilogue source);
 // this kernel keeps 128-wide tiles, the produced-A GEMMs and devices where no
@@ -56,7 +57,7 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   // The pixel producer's raw-byte ring and LUT take the room of one stage.
-  static constexpr int STAGES = (BN == 320 ? 3 : BN == 256 ? 4 : 6) - (ASRC == kAPixels ? 1 : 0);
+  static constexpr int STAGES = (BN > 256 ? 3 : BN == 256 ? 4 : 6) - (ASRC == kAPixels ? 1 : 0);
   static constexpr int EPI_WARPS = 8;
   static constexpr int STG_BYTES = 32 * 32 * 2;                // one 32x32 bf16 chunk
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;         // 2 staging chunks per warp
@@ -84,6 +85,7 @@ static_assert(GemmCfg<256, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<128, kAPixels>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<320>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(GemmCfg<320, kAMerge>::SMEM_BYTES <= 232448, "shared memory");
+static_assert(GemmCfg<288>::SMEM_BYTES <= 232448, "shared memory");
 static_assert(3 * GemmCfg<128>::STAGES + 5 <= 31, "barrier slots");
 
 // Image of packed row `row` (offsets `off`, n images) and the row's index in it.
@@ -322,7 +324,7 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
     if constexpr (ASRC == kATma) prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
     prefetch_tensormap(&tmC);
-    if constexpr (BN == 320) prefetch_tensormap(&tmB64);
+    if constexpr (BN > 256) prefetch_tensormap(&tmB64);
   }
   if (warp == 9) {
     tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
@@ -360,7 +362,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
             tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * (BN / 2));
             tma_load_2d(stage_b(stage) + (BN / 2) * C::BK * 2, &tmB, full_bar(stage), kb * C::BK,
                         p.N / 2 + nb * (BN / 2));
-          } else if constexpr (BN == 320) {
+          } else if constexpr (BN > 256) {
+            // Rows nb*BN .. +255 and the remaining BN - 256 rows (tmB64: a box
+            // of exactly that many rows).
             tma_load_2d(stage_b(stage), &tmB, full_bar(stage), kb * C::BK, nb * BN);
             tma_load_2d(stage_b(stage) + 256 * C::BK * 2, &tmB64, full_bar(stage), kb * C::BK, nb * BN + 256);
           } else {
@@ -378,8 +382,8 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
   } else if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16_f32(128, BN == 320 ? 256 : BN, false, false);
-      constexpr uint32_t idesc64 = idesc_bf16_f32(128, 64, false, false);
+      constexpr uint32_t idesc = idesc_bf16_f32(128, BN > 256 ? 256 : BN, false, false);
+      constexpr uint32_t idesc_rest = idesc_bf16_f32(128, BN > 256 ? BN - 256 : 64, false, false);
       // Descriptors are built once; a stage or K step only advances the start
       // address field (byte offset >> 4).
       const uint64_t da0 = sdesc_sw128(stage_a(0), 16, 1024);
@@ -408,9 +412,9 @@ __global__ void __launch_bounds__(GemmCfg<BN, ASRC>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < C::BK / 16; ++k) {
             umma_bf16(d_tmem, da0 + off + 2 * k, db0 + off + 2 * k, idesc, (kb | k) != 0);
-            // Rows 256..319 of B (32 KB on) into accumulator columns 256..319.
-            if constexpr (BN == 320)
-              umma_bf16(d_tmem + 256, da0 + off + 2 * k, db0 + off + ((256 * 128) >> 4) + 2 * k, idesc64,
+            // Rows 256..BN-1 of B (32 KB on) into accumulator columns 256..BN-1.
+            if constexpr (BN > 256)
+              umma_bf16(d_tmem + 256, da0 + off + 2 * k, db0 + off + ((256 * 128) >> 4) + 2 * k, idesc_rest,
                         (kb | k) != 0);
           }
           umma_commit(empty_bar(stage));
@@ -571,7 +575,7 @@ int gemm_bn(int M, int N) {
 
 bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k) {
   return make_tmap_bf16(&m->bn256, w, n, k, 256) && make_tmap_bf16(&m->bn128, w, n, k, 128) &&
-         make_tmap_bf16(&m->bn64, w, n, k, 64);
+         make_tmap_bf16(&m->bn64, w, n, k, 64) && make_tmap_bf16(&m->bn32, w, n, k, 32);
 }
 
 // 320-wide tiles where they fit one round and the 256-wide choice needs two
@@ -583,6 +587,14 @@ bool prefer_bn320(int M, int N) {
   const int tiles320 = ((M + 127) / 128) * (N / 320);
   const int tiles_pair = ((M + 255) / 256) * (N / 256);
   return tiles320 <= sms && tiles_pair > sms / 2;
+}
+
+// 288-wide tiles for widths that are a multiple of 288 but not of 256 (1152)
+// where they fit one round: 128 tiles against 288 128-wide ones (two rounds)
+// at 4096 rows, with 11 instead of 15 KB of operands per MFLOP.
+bool prefer_bn288(int M, int N) {
+  if (N % 288 != 0 || N % 256 == 0) return false;
+  return ((M + 127) / 128) * (N / 288) <= num_sms();
 }
 
 int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& tmC, int M, int N,
@@ -605,6 +617,13 @@ int launch_gemm(const CUtensorMap& tmA, const WeightMap& B, const CUtensorMap& t
   if (epi == kEpiSwiglu) {
     if (N % 256 != 0) return DS_VIT_EINVAL;
     return launch_gemm_t<256, kEpiSwiglu>(tmA, B.bn128, tmC, p, stream);
+  }
+  if ((epi == kEpiBias || epi == kEpiBiasGelu || epi == kEpiBiasResid) && prefer_bn288(M, N)) {
+    switch (epi) {
+      case kEpiBias: return launch_gemm_t<288, kEpiBias>(tmA, B.bn256, tmC, p, stream, nullptr, &B.bn32);
+      case kEpiBiasGelu: return launch_gemm_t<288, kEpiBiasGelu>(tmA, B.bn256, tmC, p, stream, nullptr, &B.bn32);
+      default: return launch_gemm_t<288, kEpiBiasResid>(tmA, B.bn256, tmC, p, stream, nullptr, &B.bn32);
+    }
   }
   // Widths that are a multiple of 128 but not of 256 (1152) take 128-wide tiles.
   if (N % 256 != 0 || gemm_bn(M, N) == 128) {

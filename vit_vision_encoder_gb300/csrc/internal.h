@@ -71,6 +71,7 @@ struct WeightMap {
   CUtensorMap bn256;   // box 256 rows
   CUtensorMap bn128;   // box 128 rows
   CUtensorMap bn64;    // box 64 rows (the last rows of a 320-row tile)
+  CUtensorMap bn32;    // box 32 rows (the last rows of a 288-row tile)
 };
 bool make_weight_map(WeightMap* m, const void* w, uint64_t n, uint64_t k);
 

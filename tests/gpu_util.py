@@ -1,4 +1,7 @@
-"""Helpers shared by the GPU tests (conversion and tolerance checks only)."""
+"""Helpers shared by the GPU tests (conversion and tolerance checks, and a
+disk cache of full oracle encodes)."""
+import glob
+import hashlib
 import itertools
 import json
 import os
@@ -112,9 +115,64 @@ def assert_within_spread(got, ref, env, what=""):
                 lim_mean=float(env["mean"]), cos=float(c.min()), stated_bound=stated)
 
 
+def _oracle_cache_key(imgs, W, cfg, n_layers):
+    """Digest of everything a default oracle encode depends on: the image
+    bytes, every weight array, the layer count, the model constants and the
+    oracle's own source files (a changed oracle never reads an old entry)."""
+    h = hashlib.sha256()
+    for im in imgs:
+        h.update(repr(im.shape).encode())
+        h.update(np.ascontiguousarray(im).tobytes())
+
+    def walk(v):
+        if isinstance(v, dict):
+            for k in sorted(v):
+                h.update(str(k).encode())
+                walk(v[k])
+        elif isinstance(v, (list, tuple)):
+            for x in v:
+                walk(x)
+        elif isinstance(v, np.ndarray):
+            h.update(repr((v.dtype.str, v.shape)).encode())
+            h.update(np.ascontiguousarray(v).tobytes())
+        else:
+            h.update(repr(v).encode())
+
+    walk(W)
+    walk(cfg)
+    h.update(repr(n_layers).encode())
+    root = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle")
+    for f in sorted(glob.glob(os.path.join(root, "*.py"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:32]
+
+
+def oracle_encode_cached(imgs, W, cfg, n_layers=None):
+    """O.encode (default evaluation) through a disk cache keyed by
+    _oracle_cache_key, in $DSVIT_ORACLE_CACHE (default ~/.cache/dsvit-oracle).
+    The cache only saves time: a missing or unreadable entry is recomputed."""
+    d = os.environ.get("DSVIT_ORACLE_CACHE", os.path.join(os.path.expanduser("~"), ".cache", "dsvit-oracle"))
+    path = os.path.join(d, _oracle_cache_key(imgs, W, cfg, n_layers) + ".npz")
+    try:
+        with np.load(path) as z:
+            return z["e"], z["offs"]
+    except (OSError, KeyError, ValueError):
+        pass
+    e, offs = O.encode(imgs, W, cfg, n_layers=n_layers)
+    try:
+        os.makedirs(d, exist_ok=True)
+        tmp = path + f".{os.getpid()}.tmp.npz"
+        np.savez(tmp, e=e, offs=offs)
+        os.replace(tmp, path)
+    except OSError:
+        pass
+    return e, offs
+
+
 def assert_end_to_end(got, imgs, W, cfg, n_layers=None, what="", env=None):
     """Free-running embeddings vs the oracle within the spread of its valid
-    evaluations (computed here, or a stored envelope ``env``)."""
+    evaluations (computed here, or a stored envelope ``env``, in which case
+    the oracle's default evaluation comes through the disk cache)."""
     box = {}
 
     def run():
@@ -124,7 +182,7 @@ def assert_end_to_end(got, imgs, W, cfg, n_layers=None, what="", env=None):
     if env is None:
         ref, env = oracle_spread(run)
     else:
-        ref = run()
+        ref, box["offs"] = oracle_encode_cached(imgs, W, cfg, n_layers=n_layers)
     return box["offs"], assert_within_spread(got, ref, env, what)
 
 

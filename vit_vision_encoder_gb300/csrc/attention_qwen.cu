@@ -17,9 +17,10 @@
 //
 // The schedule is the head-64 kernel's: one CTA = (256 query rows, head) as
 // two 128-row tiles A and B that share every K/V tile; warps 0-7 run the
-// softmax of tile A and warps 8-15 that of tile B with two threads per query
-// row (one per 64-key half, half-row maxima and sums exchanged through shared
-// memory); the exponent math of the two tiles takes turns; warp 16 loads Q
+// softmax of tile A and warps 8-15 that of tile B, each warp 16 query rows
+// with two threads per row (one per 64-key half, threads t and t + 16 through
+// the 16x32bx2 TMEM shape, half-row maxima and sums exchanged by warp
+// shuffle); the exponent math of the two tiles takes turns; warp 16 loads Q
 // once and streams K/V through a 3-stage TMA ring; warps 17 and 18 issue the
 // MMAs of tiles A and B.  The running maximum is raised only when it grows by
 // more than 8 (log2 units); the final O / l uses the same maximum, so the
@@ -72,8 +73,7 @@ enum : int {
   kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
   kBarDrain = kBarPvDone + 2,          // [2]
-  kBarXch = kBarDrain + 2,             // [2 tiles][4 quadrants]
-  kBarTurn = kBarXch + 8,              // [2]
+  kBarTurn = kBarDrain + 2,            // [2]
   kBarCount = kBarTurn + 2
 };
 static_assert(kBarCount <= 30, "barrier area");
@@ -108,19 +108,6 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
   return r;
 }
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                 "=r"(r[7])
-               : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
-               :
-               : "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
-                 "r"(r[7])
-               : "memory");
-}
 
 // 19 warps: five share one SM sub-partition's 16K registers, so 96 a thread.
 __global__ void __maxnreg__(96)
@@ -154,7 +141,6 @@ __global__ void __maxnreg__(96)
       mbar_init(bar(kBarPFull + x), 256);
       mbar_init(bar(kBarPvDone + x), 1);
       mbar_init(bar(kBarDrain + x), 1);
-      for (int q = 0; q < 4; ++q) mbar_init(bar(kBarXch + 4 * x + q), 64);
       mbar_init(bar(kBarTurn + x), 256);
     }
     fence_barrier_init();
@@ -175,7 +161,6 @@ __global__ void __maxnreg__(96)
   grid_dep_wait();
 
   __shared__ int kv_consumed[2];
-  __shared__ float xch[2][2][2][kTile];   // [exchange parity][tile][half][row]
   int kv_issued = 0;
   bool q_issued = false;
   const int colq = head * kHdPad, colk = (kHeads + head) * kHdPad, colv = (2 * kHeads + head) * kHdPad;
@@ -258,23 +243,17 @@ __global__ void __maxnreg__(96)
     // ------------------------------------------------------------ softmax (warps 0-15)
     const int x = warp >> 3;                 // query tile A (0) or B (1)
     const int qd = warp & 3;                 // TMEM lane quadrant
-    const int h = (warp >> 2) & 1;           // 64-key half of the score tile
-    const int r = qd * 32 + lane;
-    const uint32_t lane_sel = static_cast<uint32_t>(qd * 32) << 16;
-    const uint32_t tS = tmem + x * 128 + h * 64 + lane_sel;
+    const int base = qd * 32 + ((warp >> 2) & 1) * 16;   // the warp's first row
+    const int h = lane >> 4;                 // 64-key half of the score tile
+    const int r = base + (lane & 15);
+    // Addresses of the first half; the 16x32bx2 accesses put threads 16-31 on
+    // the second: scores 64 columns on, P 128 (kTmemP1 - kTmemP0), O 40 (the
+    // first half owns O columns 0..39, the second 40..71; 72..79 stay zero).
+    const uint32_t lane_sel = static_cast<uint32_t>(base) << 16;
+    const uint32_t tS = tmem + x * 128 + lane_sel;
     const uint32_t tO = tmem + kTmemO + x * 128 + lane_sel;
-    const uint32_t tP = tmem + (h ? kTmemP1 : kTmemP0) + lane_sel;
-    const uint32_t xbar = bar(kBarXch + 4 * x + qd);
-    // Both threads of a row write their half's value, arrive, wait for the
-    // phase and read the other's; slot parity e alternates, so a slot is
-    // rewritten only after its reader has arrived at the next exchange.
-    auto exchange = [&](float v, int e, float* other) {
-      xch[e & 1][x][h][r] = v;
-      mbar_arrive(xbar);
-      if (!mbar_wait(xbar, e & 1, p.status)) return false;
-      *other = xch[e & 1][x][h ^ 1][r];
-      return true;
-    };
+    const uint32_t tP = tmem + kTmemP0 + lane_sel;
+    static_assert(kTmemP1 - kTmemP0 == 128, "P halves 128 columns apart");
     const float c = p.scale_log2;
     const uint64_t c2 = f2(c, c);
     float m = -INFINITY, l = 0.f;
@@ -288,7 +267,7 @@ __global__ void __maxnreg__(96)
       tc_fence_after();
       uint32_t sr[64];
       // One load of the 64 scores that also reduces them to their maximum.
-      float m_half = tmem_ld64_max(tS, sr);
+      float m_half = tmem_ld64_max_x2<64>(tS, sr);
       tmem_wait_ld();
       m_half = tmem_after_wait(m_half);
       tc_fence_before();
@@ -311,11 +290,7 @@ __global__ void __maxnreg__(96)
         }
         m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       }
-      float m_other;
-      if (!exchange(m_half, j, &m_other)) {
-        ok = false;
-        break;
-      }
+      const float m_other = __shfl_xor_sync(0xFFFFFFFFu, m_half, 16);
       const float m_tile = fmaxf(m_half, m_other) * c;
       float m_new = m, alpha = 1.f;
       if (m_tile > m + kRescaleThreshold) {   // always true on the first tile (m = -inf)
@@ -351,31 +326,30 @@ __global__ void __maxnreg__(96)
         break;
       }
       tc_fence_after();
-      tmem_st32(tP, pk);
+      tmem_st32_x2<128>(tP, pk);
       if (j > 0 && __any_sync(0xFFFFFFFFu, alpha != 1.f)) {
-        // Half h rescales O columns [40 h, 40 h + 40) (72..79 stay zero).
+        // Half h rescales O columns [40 h, 40 h + 32) and then [40 h + 32,
+        // 40 h + 40) (for h = 1 columns 72..79, which stay zero).
         uint32_t o[32];
-        tmem_ld32(tO + h * 40, o);
+        tmem_ld32_x2<40>(tO, o);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-        tmem_st32(tO + h * 40, o);
-        if (h == 0) {
-          uint32_t o8[8];
-          tmem_ld8(tO + 32, o8);
-          tmem_wait_ld();
+        tmem_st32_x2<40>(tO, o);
+        uint32_t o8[8];
+        tmem_ld8_x2<40>(tO + 32, o8);
+        tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 8; ++i) o8[i] = __float_as_uint(__uint_as_float(o8[i]) * alpha);
-          tmem_st8(tO + 32, o8);
-        }
+        for (int i = 0; i < 8; ++i) o8[i] = __float_as_uint(__uint_as_float(o8[i]) * alpha);
+        tmem_st8_x2<40>(tO + 32, o8);
       }
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar(kBarPFull + x));
       m = m_new;
     }
-    float l_other = 0.f;
-    if (ok && exchange(l, n_kv, &l_other) && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
+    const float l_other = __shfl_xor_sync(0xFFFFFFFFu, l, 16);
+    if (ok && mbar_wait(bar(kBarPvDone + x), (n_kv - 1) & 1, p.status)) {
       tc_fence_after();
       const float inv_l = 1.f / (l + l_other);
       // Thread h = 0 writes dims 0..39, h = 1 dims 40..71: 32 columns, then
@@ -391,18 +365,18 @@ __global__ void __maxnreg__(96)
       };
       {
         uint32_t o[32];
-        tmem_ld32(tO + h * 40, o);
+        tmem_ld32_x2<40>(tO, o);
         tmem_wait_ld();
         if (qrow < len) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) put8(dst + q, o + 8 * q);
         }
       }
-      if (h == 0) {
+      {
         uint32_t o[8];
-        tmem_ld8(tO + 32, o);
+        tmem_ld8_x2<40>(tO + 32, o);         // h = 1: columns 72..79, not written
         tmem_wait_ld();
-        if (qrow < len) put8(dst + 4, o);
+        if (h == 0 && qrow < len) put8(dst + 4, o);
       }
     }
   }

@@ -342,6 +342,21 @@ __device__ __forceinline__ void tmem_st32_x2(uint32_t taddr, const uint32_t (&r)
       : "memory");
 }
 
+// 8 columns per thread, 16x32bx2 shape (see tmem_ld64_max_x2).
+template <int kHalf>
+__device__ __forceinline__ void tmem_ld8_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8], %9;"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr), "n"(kHalf));
+}
+
+template <int kHalf>
+__device__ __forceinline__ void tmem_st8_x2(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2, %3, %4, %5, %6, %7, %8, %9};" ::"r"(taddr),
+               "n"(kHalf), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+
 __device__ __forceinline__ float tmem_after_wait(float v) {
   asm volatile("mov.b32 %0, %0;" : "+f"(v));
   return v;

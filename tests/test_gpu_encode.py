@@ -174,6 +174,31 @@ def test_graph_replays_the_encode(dv, enc2):
             g.close()
 
 
+def test_graph_create_failure_keeps_nothing(dv, enc2):
+    """A recording whose encode rejects its arguments returns that error,
+    stores no handle and leaves no capture open: a direct encode right after
+    works and matches a fresh one."""
+    import ctypes as C
+    img = torch.from_numpy(WL.uniform_image(84, 84, seed=11)).cuda()
+    out = torch.zeros((4, 5120), dtype=torch.bfloat16, device="cuda")
+    ws = enc2.workspace([(84, 84)])
+    px = (C.c_void_p * 1)(img.data_ptr())
+    offs = (C.c_int64 * 2)()
+    h = C.c_void_p(7)
+    bad_h, bad_w = (C.c_int32 * 1)(85), (C.c_int32 * 1)(84)
+    rc = dv.lib.ds_vit_graph_create(enc2.handle, 0, 1, px, bad_h, bad_w, C.c_void_p(out.data_ptr()), offs,
+                                    C.c_void_p(ws.data_ptr()), ws.numel(), C.byref(h))
+    assert rc == dv.EINVAL and not h.value
+    small = (C.c_int32 * 1)(84)
+    rc = dv.lib.ds_vit_graph_create(enc2.handle, 0, 1, px, small, small, C.c_void_p(out.data_ptr()), offs,
+                                    C.c_void_p(ws.data_ptr()), 1024, C.byref(h))
+    assert rc == dv.ECAP and not h.value
+    a, _ = _run(dv, enc2, [WL.uniform_image(84, 84, seed=11)])
+    b, _ = enc2.encode([img])
+    torch.cuda.synchronize()
+    assert torch.equal(a, b) and bool((out == 0).all())
+
+
 def test_graph_host_buffers(dv, enc2):
     """The host-buffer encode recorded as a graph: both copies and the encode
     in every replay, page-locked buffers."""

@@ -23,7 +23,8 @@
 // The softmax threads of a tile read S_X from TMEM and hand the buffer back at
 // once, so the next S_X is computed while they work.  The exponent math of the
 // two tiles takes turns (A of step j, B of step j, A of step j+1, ...: an
-// mbarrier per tile), so each sub-partition runs one tile's math at full issue
+// mbarrier per tile and TMEM lane quadrant, so each SM sub-partition hands
+// over on its own), so each sub-partition runs one tile's math at full issue
 // rate while the tensor core works on the other tile; left to run together the
 // two tiles fall into step and their math serialises with the MMAs (1.5x
 // slower).  The running row maximum m
@@ -68,8 +69,9 @@ enum : int {
   kBarPFull = kBarSFree + 2,           // [2]
   kBarPvDone = kBarPFull + 2,          // [2]
   kBarDrain = kBarPvDone + 2,          // [2]
-  kBarTurn = kBarDrain + 2,            // [2]: tile X finished the math of a step
-  kBarCount = kBarTurn + 2
+  kBarTurn = kBarDrain + 2,            // [2 tiles][4 quadrants]: the quadrant's warps of tile X
+                                       // finished the math of a step
+  kBarCount = kBarTurn + 8
 };
 static_assert(kBarCount <= 30, "barrier area");
 
@@ -143,7 +145,7 @@ __global__ void __maxnreg__(96)
       mbar_init(bar(kBarPFull + x), 256);
       mbar_init(bar(kBarPvDone + x), 1);
       mbar_init(bar(kBarDrain + x), 1);
-      mbar_init(bar(kBarTurn + x), 256);
+      for (int q = 0; q < 4; ++q) mbar_init(bar(kBarTurn + 4 * x + q), 64);
     }
     fence_barrier_init();
   }
@@ -261,7 +263,7 @@ __global__ void __maxnreg__(96)
       // Take turns: A's step j after B's step j-1, B's step j after A's step j.
       if (x == 1 || j > 0) {
         // The other tile's math takes about a microsecond: poll it sparingly.
-        if (!mbar_wait_sleepy(bar(kBarTurn + (x ^ 1)), (x == 1 ? j : j - 1) & 1, 200u, p.status)) {
+        if (!mbar_wait_sleepy(bar(kBarTurn + 4 * (x ^ 1) + qd), (x == 1 ? j : j - 1) & 1, 200u, p.status)) {
           ok = false;
           break;
         }
@@ -297,7 +299,7 @@ __global__ void __maxnreg__(96)
         acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
-      mbar_arrive(bar(kBarTurn + x));         // the other tile's turn
+      mbar_arrive(bar(kBarTurn + 4 * x + qd));   // the other tile's turn on this sub-partition
       const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float s0, s1;
       f2_split(s2, s0, s1);

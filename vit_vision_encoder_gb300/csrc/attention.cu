@@ -262,8 +262,7 @@ __global__ void __maxnreg__(96)
       mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
       // Take turns: A's step j after B's step j-1, B's step j after A's step j.
       if (x == 1 || j > 0) {
-        // The other tile's math takes about a microsecond: poll it sparingly.
-        if (!mbar_wait_sleepy(bar(kBarTurn + 4 * (x ^ 1) + qd), (x == 1 ? j : j - 1) & 1, 200u, p.status)) {
+        if (!mbar_wait(bar(kBarTurn + 4 * (x ^ 1) + qd), (x == 1 ? j : j - 1) & 1, p.status)) {
           ok = false;
           break;
         }

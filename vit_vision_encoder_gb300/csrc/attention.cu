@@ -260,13 +260,6 @@ __global__ void __maxnreg__(96)
       m_half = tmem_after_wait(m_half);
       tc_fence_before();
       mbar_arrive(bar(kBarSFree + x));       // the MMA may overwrite S_X now
-      // Take turns: A's step j after B's step j-1, B's step j after A's step j.
-      if (x == 1 || j > 0) {
-        if (!mbar_wait(bar(kBarTurn + 4 * (x ^ 1) + qd), (x == 1 ? j : j - 1) & 1, p.status)) {
-          ok = false;
-          break;
-        }
-      }
       const int kv_valid = len - j * kTile - h * 64;
       if (kv_valid < 64) {
         // Keys past the image: masked, and the maximum taken over the rest.
@@ -278,6 +271,8 @@ __global__ void __maxnreg__(96)
         }
         m_half = fmaxf(max3(mx[0], mx[1], mx[2]), mx[3]);
       }
+      // The row's maximum (a shuffle with the other half's thread) and the
+      // rescale decision need no turn: only the exponent loop takes turns.
       const float m_other = __shfl_xor_sync(0xFFFFFFFFu, m_half, 16);
       // Both threads of the row derive the same m_new and alpha.
       const float m_tile = fmaxf(m_half, m_other) * c;
@@ -286,19 +281,32 @@ __global__ void __maxnreg__(96)
         m_new = m_tile;
         alpha = ex2_approx(m - m_new);
       }
+      // Take turns: A's step j after B's step j-1, B's step j after A's step j.
+      if (x == 1 || j > 0) {
+        if (!mbar_wait(bar(kBarTurn + 4 * (x ^ 1) + qd), (x == 1 ? j : j - 1) & 1, p.status)) {
+          ok = false;
+          break;
+        }
+      }
       const uint64_t nm2 = f2(-m_new, -m_new);
-      uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
-      uint32_t pk[32];
+      // Only the exponents take the turn; the sums and bf16 packs follow it.
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const uint64_t t = f2_fma(f2(__uint_as_float(sr[2 * i]), __uint_as_float(sr[2 * i + 1])), c2, nm2);
         float t0, t1;
         f2_split(t, t0, t1);
-        const float p0 = ex2_approx(t0), p1 = ex2_approx(t1);
+        sr[2 * i] = __float_as_uint(ex2_approx(t0));
+        sr[2 * i + 1] = __float_as_uint(ex2_approx(t1));
+      }
+      mbar_arrive(bar(kBarTurn + 4 * x + qd));   // the other tile's turn on this sub-partition
+      uint64_t acc[4] = {f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f), f2(0.f, 0.f)};
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = __uint_as_float(sr[2 * i]), p1 = __uint_as_float(sr[2 * i + 1]);
         acc[i & 3] = f2_add(acc[i & 3], f2(p0, p1));
         pk[i] = pack_bf16x2(p0, p1);
       }
-      mbar_arrive(bar(kBarTurn + 4 * x + qd));   // the other tile's turn on this sub-partition
       const uint64_t s2 = f2_add(f2_add(acc[0], acc[1]), f2_add(acc[2], acc[3]));
       float s0, s1;
       f2_split(s2, s0, s1);

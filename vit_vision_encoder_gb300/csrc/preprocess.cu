@@ -5,19 +5,20 @@
 // 295,936, at most 1,024 image tokens, no aspect clamp; Lucebox "Image input":
 // bicubic resizing that matches Pillow byte for byte).
 //
-// The plan is host integer/float64 code.  On the device: one kernel builds the
-// per-output-index filter tables of both axes in float64 (every operation an
-// explicitly rounded intrinsic, so no contraction changes a weight), one runs
-// the horizontal pass (rows of the input -> Wr columns, into rows padded to 16
-// bytes) and one the vertical pass, writing the canvas directly (gray outside
-// the resized image).  Each pass rounds to uint8 as
-// (2^21 + sum pixel * weight) >> 22, clamped.  The fast passes: horizontal,
-// a block stages the input span of 128 output pixels for 8 rows in shared
-// memory and each thread keeps its pixel's (at most 15) weights in registers
-// and reads its window as words; vertical, every byte of an output row has
-// the same weights, so a thread makes 16 consecutive bytes from one 16-byte
-// load per tap.  The per-pixel kernels remain for wider filters and
-// unaligned sources.
+// The plan is host integer/float64 code.  On the device: the filter tables of
+// both axes in float64 (every operation an explicitly rounded intrinsic, so no
+// contraction changes a weight; several output indices per warp), stored as
+// tap-major ints and in byte planes for dp4a; the horizontal pass (rows of the
+// input -> Wr columns, into rows padded to 16 bytes) and the vertical pass,
+// writing the canvas directly (gray outside the resized image).  Each pass
+// rounds to uint8 as (2^21 + sum pixel * weight) >> 22, clamped.  The planar
+// passes take four taps' products per dp4a in each weight byte plane (exact
+// in 32-bit integers): horizontally a block stages its input span split into
+// R, G, B planes; vertically a thread transposes 4 rows x 8 bytes so that a
+// word holds one output byte's four taps.  The horizontal pass builds the
+// height's tables in leading blocks and stages its pixels before it waits for
+// the width's tables (programmatic dependent launch).  The per-pixel kernels
+// remain for wider filters and unaligned sources.
 #include "internal.h"
 #include "ptx.cuh"
 

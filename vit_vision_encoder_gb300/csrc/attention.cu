@@ -21,13 +21,15 @@
 //   S_X = Q_X K_j^T     (M 128, N 128, K 64)  smem x smem -> TMEM
 //   O_X += P_X V_j      (M 128, N 64,  K 128) TMEM x smem -> TMEM
 // The softmax threads of a tile read S_X from TMEM and hand the buffer back at
-// once, so the next S_X is computed while they work.  The exponent math of the
-// two tiles takes turns (A of step j, B of step j, A of step j+1, ...: an
+// once, so the next S_X is computed while they work.  The exponents of the
+// two tiles take turns (A of step j, B of step j, A of step j+1, ...: an
 // mbarrier per tile and TMEM lane quadrant, so each SM sub-partition hands
-// over on its own), so each sub-partition runs one tile's math at full issue
+// over on its own), so each sub-partition runs one tile's exponents at full
 // rate while the tensor core works on the other tile; left to run together the
 // two tiles fall into step and their math serialises with the MMAs (1.5x
-// slower).  The running row maximum m
+// slower).  Only the exponents take the turn: the row maximum and rescale
+// decision come before it, the row sums and bf16 packs after its hand-off.
+// The running row maximum m
 // (exp2 domain) is raised only when a tile's maximum exceeds it by more than
 // 8, so P = exp2(s - m) stays below 2^8 and O is rescaled (in TMEM, by
 // exp2(m_old - m_new)) rarely; the final O / l uses the same m, so the result

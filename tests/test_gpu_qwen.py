@@ -4,7 +4,8 @@ oracle (oracle/qwen.py): every step recomputed from the GPU's own input to it
 primary merger, the DeepStack merger of block 8) within the encode's step
 bound, and the free-running outputs within the oracle's own summation-order
 spread.  Grids: 2x2 merged (one partial query tile), 7x7 (ragged tiles),
-16x12; 9 blocks so that the first DeepStack tap is reached."""
+16x12; 9 blocks so that the first DeepStack tap is reached; and the
+benchmarked 1024x1024 image with all 27 blocks, every step teacher-forced."""
 import math
 
 import numpy as np
@@ -119,6 +120,32 @@ def test_qwen_full_grid_block_repeatable(dv, wq):
         assert_parity(bits_of(bl[1]), ref, what="block 0 at 4096 patches")
     finally:
         e.close()
+
+
+def test_qwen_full_size_every_block(dv):
+    """The benchmarked configuration: 1024x1024 (4096 patches), all 27 blocks
+    of the tower.  Every block teacher-forced on every row, the primary merger
+    and the three DeepStack mergers (taps after blocks 8, 16 and 24) from the
+    GPU's own inputs."""
+    cfg = WL.QWEN_MODEL
+    n = cfg["n_layers"]
+    w = WL.make_weights_qwen(n)
+    e = dv.QwenEncoder(dv.weights_to_device(w), cfg)
+    try:
+        img = WL.uniform_image(1024, 1024, seed=2048)
+        out, deep, blocks = e.encode(torch.from_numpy(img).cuda(), dump=True)
+        torch.cuda.synchronize()
+        bl = blocks.cpu()
+    finally:
+        e.close()
+    gy, gx = Q.patch_order(64, 64)
+    for l in range(n):
+        ref = Q.block(bits_of(bl[l]), w["layers"][l], cfg, gy, gx)
+        assert_parity(bits_of(bl[l + 1]), ref, what=f"block {l} at 4096 patches")
+    assert_parity(host(out), Q.merger(bits_of(bl[n]), w["merger"], cfg), what="merger at 4096 patches")
+    for k, tap in enumerate(cfg["taps"]):
+        assert_parity(host(deep[k]), Q.merger(bits_of(bl[tap]), w["deepstack"][k], cfg),
+                      what=f"deepstack {tap} at 4096 patches")
 
 
 def test_qwen_peaked_attention(dv, wq):

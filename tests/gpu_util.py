@@ -216,3 +216,28 @@ def assert_steps_teacher_forced(imgs, W, cfg, blocks, fnorm, out, layers, rows=N
                         for i in range(len(imgs))])
     t = np.arange(A.shape[0]) if toks is None else np.asarray(toks)
     assert_parity(out.float().cpu().numpy()[t], O.merger(A[t], W), what="merger")
+
+
+def sample_rows(seqlens, per_image, seed):
+    """Rows of a packed batch to check: per image its first and last row, the
+    first row of its last 128-row query tile and `per_image` random rows."""
+    rng = np.random.default_rng(seed)
+    starts = np.concatenate([[0], np.cumsum(seqlens)])
+    rows = []
+    for a, n in zip(starts[:-1], seqlens):
+        pick = {0, n - 1, 128 * ((n - 1) // 128)}
+        pick |= {int(r) for r in rng.choice(n, min(n, per_image), replace=False)}
+        rows += [int(a) + r for r in sorted(pick)]
+    return np.array(rows)
+
+
+def sample_tokens(offs, per_image, seed):
+    """Merged tokens to check: per image its first, middle and last token and
+    `per_image` random ones."""
+    rng = np.random.default_rng(seed)
+    toks = []
+    for a, b in zip(offs[:-1], offs[1:]):
+        n = int(b - a)
+        pick = {0, n // 2, n - 1} | {int(t) for t in rng.choice(n, min(n, per_image), replace=False)}
+        toks += [int(a) + t for t in sorted(pick)]
+    return np.array(toks)

@@ -18,7 +18,8 @@ import pytest
 
 import oracle as O
 import workloads as WL
-from gpu_util import (assert_end_to_end, assert_steps_teacher_forced, dev, host, stored_spread)
+from gpu_util import (assert_end_to_end, assert_steps_teacher_forced, dev, host, sample_rows, sample_tokens,
+                      stored_spread)
 
 pytestmark = pytest.mark.gpu
 
@@ -267,31 +268,6 @@ def test_min_image_full_depth(dv, enc32, w32):
                       env=stored_spread("min"))
 
 
-def _sample_rows(seqlens, per_image, seed):
-    """Rows of a packed batch to check: per image its first and last row, the
-    first row of its last 128-row query tile and `per_image` random rows."""
-    rng = np.random.default_rng(seed)
-    starts = np.concatenate([[0], np.cumsum(seqlens)])
-    rows = []
-    for a, n in zip(starts[:-1], seqlens):
-        pick = {0, n - 1, 128 * ((n - 1) // 128)}
-        pick |= {int(r) for r in rng.choice(n, min(n, per_image), replace=False)}
-        rows += [int(a) + r for r in sorted(pick)]
-    return np.array(rows)
-
-
-def _sample_tokens(offs, per_image, seed):
-    """Merged tokens to check: per image its first, middle and last token and
-    `per_image` random ones."""
-    rng = np.random.default_rng(seed)
-    toks = []
-    for a, b in zip(offs[:-1], offs[1:]):
-        n = int(b - a)
-        pick = {0, n // 2, n - 1} | {int(t) for t in rng.choice(n, min(n, per_image), replace=False)}
-        toks += [int(a) + t for t in sorted(pick)]
-    return np.array(toks)
-
-
 @pytest.fixture(scope="module")
 def max_run(dv, enc32):
     """The 1344x1344 image through ds_vit_encode (plain) and through the debug
@@ -315,9 +291,9 @@ def test_max_image_all_blocks(dv, max_run, w32):
     and sampled merged tokens, each recomputed from the GPU's own inputs."""
     img, out, offs, blocks, fnorm = max_run
     assert offs[-1] == 1024
-    rows = _sample_rows([9216], 96, seed=7)
+    rows = sample_rows([9216], 96, seed=7)
     assert_steps_teacher_forced([img], w32, WL.MODEL, blocks, fnorm, out, layers=range(32),
-                                rows=rows, toks=_sample_tokens(offs, 8, seed=8))
+                                rows=rows, toks=sample_tokens(offs, 8, seed=8))
 
 
 def test_max_image_free_running(dv, max_run, w32):
@@ -337,9 +313,9 @@ def test_aspect_image_all_blocks_and_free_running(dv, enc32, w32):
     img = WL.workload_images("aspect")[0]
     out, offs, blocks, fnorm = _run(dv, enc32, [img], dump=True)
     assert offs[-1] == 512
-    rows = np.union1d(_sample_rows([4608], 24, seed=9), [23, 24, 4584, 4600])
+    rows = np.union1d(sample_rows([4608], 24, seed=9), [23, 24, 4584, 4600])
     assert_steps_teacher_forced([img], w32, WL.MODEL, blocks, fnorm, out, layers=range(32),
-                                rows=rows, toks=_sample_tokens(offs, 6, seed=10))
+                                rows=rows, toks=sample_tokens(offs, 6, seed=10))
     del blocks, fnorm
     assert_end_to_end(host(out), [img], w32, WL.MODEL, what="2688x336 free running",
                       env=stored_spread("aspect"))
@@ -367,7 +343,7 @@ def test_batch16_full_size(dv, enc32, w32):
     assert offs[-1] == 6076
     del d
     assert_steps_teacher_forced(imgs, w32, WL.MODEL, blocks, fnorm, out, layers=range(32),
-                                rows=_sample_rows(seqlens, 4, seed=11), toks=_sample_tokens(offs, 1, seed=12))
+                                rows=sample_rows(seqlens, 4, seed=11), toks=sample_tokens(offs, 1, seed=12))
 
 
 # ------------------------------------------------------------------ overlay

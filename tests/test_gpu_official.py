@@ -3,7 +3,8 @@ RMSNorm and SwiGLU; Step 3: the half-vector RoPE pairing on [h*f, w*f];
 Step 1 item 6: pixels to [-1, 1]) against the oracle computing that variant
 directly: the RMSNorm and SwiGLU kernels alone, then whole encodes with every
 step teacher-forced and the free-running output within the oracle's own
-summation-order spread."""
+summation-order spread; and the benchmarked 1344x1344 image at 32 layers
+with sampled rows of every block teacher-forced."""
 import math
 
 import numpy as np
@@ -11,7 +12,8 @@ import pytest
 
 import oracle as O
 import workloads as WL
-from gpu_util import assert_end_to_end, assert_steps_teacher_forced, dev, host, rand_bits, rel_err
+from gpu_util import (assert_end_to_end, assert_steps_teacher_forced, dev, host, rand_bits, rel_err, sample_rows,
+                      sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -92,3 +94,20 @@ def test_official_differs_from_default(dv, enc2, w2):
     ref_default, _ = O.encode([img], w2 | {"layers": [dict(L, fc1_w=L["fc1_w"][:4096], fc1_b=L["fc1_b"][:4096])
                                                       for L in w2["layers"]]}, WL.MODEL)
     assert np.abs(host(out) - ref_default).max() > 0.05
+
+
+def test_official_full_size_every_block(dv):
+    """The benchmarked configuration: 1344x1344 (9216 patches), 32 layers of
+    the variant.  Sampled query rows of every block (each image's first and
+    last row, its last query tile's first row and 96 random rows) and sampled
+    merged tokens, each recomputed from the GPU's own inputs."""
+    w = WL.make_weights_official(32)
+    e = dv.Encoder(dv.weights_to_device(w), WL.MODEL_OFFICIAL)
+    try:
+        img = WL.workload_images("max")[0]
+        out, offs, blocks, fnorm = _run(dv, e, [img])
+    finally:
+        e.close()
+    assert offs[-1] == 1024
+    assert_steps_teacher_forced([img], w, WL.MODEL_OFFICIAL, blocks, fnorm, out, layers=range(32),
+                                rows=sample_rows([9216], 96, seed=13), toks=sample_tokens(offs, 8, seed=14))

@@ -590,11 +590,14 @@ def run_profile_case(case: str):
     import vit_vision_encoder_gb300 as dv
     torch.cuda.set_device(0)
     rng = np.random.default_rng(0)
-    if case == "encode":
+    if case in ("encode", "min-encode"):
+        # The 1344x1344 image, or the 546x546 one (1521 patches, 169 tokens).
         W = WL.make_weights(N_LAYERS)
         enc = dv.Encoder(dv.weights_to_device(W), WL.MODEL)
-        img = torch.from_numpy(WL.workload_images(WORKLOAD)[0]).cuda()
-        out = torch.empty((N_TOK, 5120), dtype=torch.bfloat16, device="cuda")
+        name = WORKLOAD if case == "encode" else "min"
+        img = torch.from_numpy(WL.workload_images(name)[0]).cuda()
+        T = enc.tokens([(int(img.shape[0]), int(img.shape[1]))])
+        out = torch.empty((T, 5120), dtype=torch.bfloat16, device="cuda")
         run = lambda: enc.encode([img], out=out)
     elif case == "overlay":
         # One 1,058-row span into the 4096 x 5120 prompt at the seeded base.

@@ -180,11 +180,15 @@ int ds_vit_preprocess_workspace_bytes(const ds_vit_plan* plan, size_t* bytes);
  * Bicubic (Keys, a = -0.5, support 2 widened by the reduction factor), weights
  * in float64 normalised per output pixel and rounded to 22 fraction bits;
  * horizontal pass then vertical pass, each rounded and clamped to uint8
- * ((2^21 + sum) >> 22); a pass whose size does not change is skipped.  The
- * canvas is written completely.  `plan` must equal ds_vit_plan_image(H, W)
- * (DS_VIT_EINVAL otherwise); ws: device workspace of at least
- * ds_vit_preprocess_workspace_bytes (DS_VIT_ECAP otherwise).  Pixel, canvas
- * and workspace memory stay caller-owned; nothing is written on an error.
+ * ((2^21 + sum) >> 22); a pass whose size does not change is skipped.  This
+ * is the separable fixed-point scheme Pillow documents for 8-bit images;
+ * agreement with Pillow itself is not tested here.  The canvas is written
+ * completely.  `plan` must equal ds_vit_plan_image(H, W) (DS_VIT_EINVAL
+ * otherwise); ws: device workspace, 256-byte aligned (DS_VIT_EINVAL
+ * otherwise), of at least ds_vit_preprocess_workspace_bytes (DS_VIT_ECAP
+ * otherwise); pixels need no alignment (a 16-byte aligned image takes the
+ * faster passes).  Pixel, canvas and workspace memory stay caller-owned;
+ * nothing is written on an error.
  */
 int ds_vit_preprocess(const ds_vit_plan* plan, const uint8_t* pixels, void* canvas, void* ws,
                       size_t ws_bytes, void* stream);
